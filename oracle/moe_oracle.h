@@ -1,0 +1,101 @@
+/*
+ * moe_oracle.h -- plain single-threaded CPU oracle for MoE token dispatch / combine.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link or
+ * call this code; only the test suite, the package's smoke check and the
+ * benchmark's CPU-baseline leg use it.  It shares no code with the CUDA
+ * library (include/moe_ep.h) and neither side includes the other.
+ *
+ * What is computed (sources: "Inside the Nebius + PyTorch DeepSeek V3 recipe",
+ * section "Mixture-of-experts and wide expert parallelism": dispatch sends each
+ * token to its top-K experts, which are partitioned across EP ranks, combine
+ * returns the expert outputs to the tokens' original positions; Hybrid-EP
+ * news article (cryptojournalpost, Feb 2 2026), sections "Technical
+ * Structure" and "Availability and Integration": dispatch and combine
+ * operators, worst-case preallocated receive buffers; "MoE / Hybrid-EP
+ * Validation", section "FP8 dispatch restriction": dispatch may carry FP8).
+ * The pages give no layout, ordering or quantisation formula; the readings
+ * used here are:
+ *
+ *   - experts are split into R contiguous blocks of m = E/R; rank(e) = e / m;
+ *   - a token is sent once per destination rank; within the packed receive
+ *     buffer rows are ordered by (primary expert, token), the primary expert
+ *     of (t, r) being the smallest expert id of token t that lives on rank r;
+ *   - expert-major rows (the y layout) are ordered by (expert, t, k);
+ *   - FP8 is OCP E4M3 (bias 7, max 448, no inf) with one fp32 scale per
+ *     1x128 block: s = amax / 448 (fp32 RN), q = e4m3_rne_satfinite(x / s);
+ *     an all-zero block gives s = 0 and q = 0x00;
+ *   - combine: acc = 0; for k ascending, acc = fma(w[t,k], y, acc) in fp32;
+ *     out = bf16_rne(acc).
+ *
+ * Every array is host memory, row-major, owned by the caller.  Return value:
+ * 0 on success, otherwise a bitwise OR of MOE_REF_ERR_* flags.  The oracle
+ * never allocates more than O(E) scratch and never aborts.
+ *
+ * Parity pins: every function here is pinned by tests that do not call it
+ * to compute their expected values (brute force, closed forms, library
+ * special cases, invariants); none is "parity unpinned".
+ */
+#ifndef MOE_ORACLE_H
+#define MOE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_REF_OK              0
+#define MOE_REF_ERR_ARG         1   /* bad sizes or null pointers           */
+#define MOE_REF_ERR_EXPERT_ID   2   /* an id outside [-1, E) was seen        */
+#define MOE_REF_ERR_CAPACITY    4   /* more (t, r) pairs than capacity rows  */
+
+/* fp32 -> bf16, round to nearest, ties to even (IEEE 754 binary32 -> bfloat16). */
+uint16_t moe_ref_bf16_encode(float v);
+float    moe_ref_bf16_decode(uint16_t b);
+
+/* fp32 -> OCP FP8 E4M3 ("fn" variant), round to nearest even, saturating to
+ * +-448; NaN -> 0x7F; the sign of zero is kept. */
+uint8_t  moe_ref_e4m3_encode(float v);
+float    moe_ref_e4m3_decode(uint8_t q);
+
+/* Routing layout.  Inputs: topk_idx [T,K] (-1 = masked entry), topk_w [T,K]
+ * (may be NULL: expert_weight is then left untouched).  Outputs (all caller
+ * owned): tokens_per_expert[E], expert_offset[E+1], tokens_per_rank[R],
+ * rank_offset[R+1], recv_expert_offset[E+1], recv_slot[T,R] (-1 = token not
+ * sent to that rank), expert_slot[T,K] (-1 = masked), recv_src_token
+ * [capacity] (-1 past the last used row), expert_src_row[T*K] and
+ * expert_weight[T*K] (-1 / 0 past the last valid entry).  Ids outside
+ * [-1, E) are flagged and treated as masked. */
+int moe_ref_layout(const int32_t* topk_idx, const float* topk_w,
+                   int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity,
+                   int32_t* tokens_per_expert, int32_t* expert_offset,
+                   int32_t* tokens_per_rank, int32_t* rank_offset,
+                   int32_t* recv_expert_offset, int32_t* recv_slot,
+                   int32_t* expert_slot, int32_t* recv_src_token,
+                   int32_t* expert_src_row, float* expert_weight);
+
+/* bf16 dispatch: recv_x[recv_slot[t,r], :] = x[t, :] for every recv_slot >= 0.
+ * x [T,H] and recv_x [capacity,H] hold bf16 bit patterns. */
+int moe_ref_dispatch_bf16(const uint16_t* x, int32_t T, int32_t H, int32_t R,
+                          const int32_t* recv_slot, int64_t capacity,
+                          uint16_t* recv_x);
+
+/* FP8 dispatch: per token and 128-column block, scale and E4M3 codes as
+ * described above, written to every destination row.  H % 128 == 0.
+ * recv_q [capacity,H] bytes, recv_scales [capacity,H/128] fp32. */
+int moe_ref_dispatch_fp8(const uint16_t* x, int32_t T, int32_t H, int32_t R,
+                         const int32_t* recv_slot, int64_t capacity,
+                         uint8_t* recv_q, float* recv_scales);
+
+/* Combine: out[t,:] = bf16_rne( fp32 fma chain over k ascending of
+ * topk_w[t,k] * y[expert_slot[t,k], :] ), skipping expert_slot < 0.
+ * y [n_rows,H] bf16 bits (expert-major), out [T,H] bf16 bits. */
+int moe_ref_combine(const uint16_t* y, int64_t n_rows, int32_t T, int32_t K,
+                    int32_t H, const int32_t* expert_slot, const float* topk_w,
+                    uint16_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_ORACLE_H */
