@@ -1,0 +1,449 @@
+#!/usr/bin/env python
+"""Benchmark of the MoE dispatch / combine hot path on one GB300 (or N replicas).
+
+One step = dispatch layout (2 kernels) -> bf16 dispatch -> combine over the
+DeepSeek-V3-shaped workload: 4096 tokens, hidden 7168, 256 experts over 8
+virtual ranks, top-8 (seeded synthetic routing and activations).  Inputs are
+resident in HBM; L2 is flushed (a 256 MB write) between timed steps, outside
+the CUDA-event brackets.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (single-threaded C) on bounded samples
+of the same workload -- the only reference there is for this path.
+Under torchrun (N > 1) each rank runs an independent replica (weak scaling,
+no collective on the data path); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "dispatch / combine HBM GB/s and tokens/s on 1 GB300, % of HBM roofline"
+WORKLOAD = "dsv3"
+L2_FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------ byte accounting
+
+def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
+    """Minimum HBM bytes of each operator: every input byte read once, every
+    output byte written once (x is read once, not once per destination)."""
+    layout = 4 * T * K * 2 + 4 * T * R + 4 * T * K * 3 + 4 * capacity + 4 * (3 * E + 2 * R + 4)
+    dispatch = 2 * T * H + 2 * H * n_pairs + 4 * T * R
+    dispatch_fp8 = 2 * T * H + n_pairs * (H + 4 * (H // 128)) + 4 * T * R
+    combine = 2 * H * n_valid + 2 * T * H + 8 * T * K
+    return {"layout": layout, "dispatch": dispatch, "dispatch_fp8": dispatch_fp8, "combine": combine}
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def committed_traffic(kernel_file: str, profile_name: str):
+    """DRAM bytes per launch from a committed ncu summary, or None if the
+    summary is missing or the kernel source changed since it was taken."""
+    prof = os.path.join(ROOT, "profiles", profile_name)
+    src = os.path.join(ROOT, "combine_moe_dispatch_02_gb300", "csrc", kernel_file)
+    if not os.path.exists(prof):
+        return None
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    vals = {}
+    for line in open(prof):
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != sha:
+        return None
+    try:
+        return int(float(vals["dram_bytes_per_full_launch"]))
+    except (KeyError, ValueError):
+        return None
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    from combine_moe_dispatch_02_gb300 import build as cuda_build
+    from combine_moe_dispatch_02_gb300 import ep
+    from combine_moe_dispatch_02_gb300.inputs import WORKLOADS, make_inputs
+
+    cuda_build.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=rank)
+    T, H, E, R, K = wl.T, wl.H, wl.E, wl.R, wl.K
+
+    L = ep.Layout(T, K, E, R, device=dev)
+    x = inp.x.to(dev)
+    idx = inp.topk_idx.to(dev)
+    w = inp.topk_w.to(dev)
+    y = inp.y.to(dev)
+    recv, _ = ep.alloc_recv(L, H, False, device=dev)
+    recv8, scales8 = ep.alloc_recv(L, H, True, device=dev)
+    out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(evs=None):
+        if evs:
+            evs[0].record(stream)
+        ep.moe_dispatch_layout(idx, w, E, R, L, stream)
+        if evs:
+            evs[1].record(stream)
+        ep.moe_dispatch(x, L, False, recv, None, stream)
+        if evs:
+            evs[2].record(stream)
+        ep.moe_combine(y, L, w, out, stream)
+        if evs:
+            evs[3].record(stream)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        step()
+    torch.cuda.synchronize(dev)
+    st, flags = ep.moe_layout_read_status(L, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} ({ep.moe_status_string(st)}) flags {flags:#x}")
+    n_pairs = int(L.rank_offset[R].item())
+    n_valid = int(L.expert_offset[E].item())
+    ab = algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, L.capacity)
+    step_bytes = ab["layout"] + ab["dispatch"] + ab["combine"]
+
+    events = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    for s in range(args.steps):
+        flush.fill_(s)            # L2 flush, outside the event brackets
+        step(events[s])
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    t_wall = time.perf_counter() - t_wall0
+    clocks = sampler.stop()
+    st, flags = ep.moe_layout_read_status(L, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timed steps")
+
+    lay = [e[0].elapsed_time(e[1]) for e in events]
+    dis = [e[1].elapsed_time(e[2]) for e in events]
+    com = [e[2].elapsed_time(e[3]) for e in events]
+    tot = [e[0].elapsed_time(e[3]) for e in events]
+    ms_step = statistics.mean(tot)
+    if world > 1:
+        t = torch.tensor([ms_step], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_step = float(t.item())
+
+    # FP8 dispatch, timed the same way (secondary figure)
+    ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 3))]
+    for e in ev8:
+        flush.fill_(3)
+        e[0].record(stream)
+        ep.moe_dispatch(x, L, True, recv8, scales8, stream)
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    dis8 = [e[0].elapsed_time(e[1]) for e in ev8]
+
+    e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if rank == 0 else None
+
+    peak, peak_kind = measured_peaks()
+    com_ms = statistics.mean(com)
+    achieved = ab["combine"] / (com_ms * 1e-3) / 1e9
+    gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
+    result = {
+        "metric": METRIC,
+        "value": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) activations, softmax top-8 routing of N(0,1) logits)",
+        "config": {"workload": "DeepSeek-V3 shape: 4096 tokens, hidden 7168, 256 experts / 8 virtual ranks, top-8",
+                   "T": T, "H": H, "E": E, "R": R, "K": K, "n_pairs": n_pairs, "capacity": L.capacity,
+                   "step": "layout + bf16 dispatch + combine", "l2": "flushed (256 MB write) between steps",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
+        "ops": {
+            "layout": {"us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"]},
+            "dispatch_bf16": {"us": round(statistics.mean(dis) * 1e3, 2), "bytes": ab["dispatch"],
+                              "GB/s": round(gbps(ab["dispatch"], statistics.mean(dis)), 1),
+                              "frac": round(gbps(ab["dispatch"], statistics.mean(dis)) / peak, 4),
+                              "tokens_per_s": round(T / (statistics.mean(dis) * 1e-3), 1)},
+            "combine": {"us": round(com_ms * 1e3, 2), "bytes": ab["combine"], "GB/s": round(achieved, 1),
+                        "frac": round(achieved / peak, 4), "tokens_per_s": round(T / (com_ms * 1e-3), 1)},
+            "dispatch_fp8": {"us": round(statistics.mean(dis8) * 1e3, 2), "bytes": ab["dispatch_fp8"],
+                             "GB/s": round(gbps(ab["dispatch_fp8"], statistics.mean(dis8)), 1),
+                             "frac": round(gbps(ab["dispatch_fp8"], statistics.mean(dis8)) / peak, 4)},
+        },
+        "roofline": {"bound": "hbm", "kernel": "combine_kernel<8>", "achieved": round(achieved, 1),
+                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
+                     else "fallback 6.8 TB/s",
+                     "traffic": committed_traffic("combine.cu", "combine_dsv3_ncu.md"),
+                     "algorithmic_bytes": ab["combine"]},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks,
+        "wall_s_timed_region": round(t_wall, 3),
+    }
+    if e2e is not None:
+        result["e2e"] = e2e
+    return result
+
+
+def run_e2e(args, inp, L, dev, ab, step_bytes):
+    """Same step through the public API with host buffers: pinned host ->
+    device copies of the inputs, the three calls, device -> host copy of the
+    combine output and the per-expert counts, all inside the timed region."""
+    import torch
+    from combine_moe_dispatch_02_gb300 import ep
+    wl = inp.wl
+    hx = inp.x.pin_memory()
+    hidx = inp.topk_idx.pin_memory()
+    hw = inp.topk_w.pin_memory()
+    hy = inp.y.pin_memory()
+    hout = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
+    hcnt = torch.empty(wl.E, dtype=torch.int32).pin_memory()
+    x = torch.empty_like(inp.x, device=dev)
+    idx = torch.empty_like(inp.topk_idx, device=dev)
+    w = torch.empty_like(inp.topk_w, device=dev)
+    y = torch.empty_like(inp.y, device=dev)
+    out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
+    recv, _ = ep.alloc_recv(L, wl.H, False, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(3, min(args.steps // 10, 50))
+
+    def one():
+        x.copy_(hx, non_blocking=True)
+        idx.copy_(hidx, non_blocking=True)
+        w.copy_(hw, non_blocking=True)
+        y.copy_(hy, non_blocking=True)
+        ep.moe_dispatch_layout(idx, w, wl.E, wl.R, L, stream)
+        ep.moe_dispatch(x, L, False, recv, None, stream)
+        ep.moe_combine(y, L, w, out, stream)
+        hout.copy_(out, non_blocking=True)
+        hcnt.copy_(L.tokens_per_expert, non_blocking=True)
+
+    for _ in range(3):
+        one()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    h2d = hx.numel() * 2 + hidx.numel() * 4 + hw.numel() * 4 + hy.numel() * 2
+    d2h = hout.numel() * 2 + hcnt.numel() * 4
+    return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+
+
+# ------------------------------------------------------------ CPU baselines
+
+def oracle_step_fn(wl, inp, T_s):
+    """One oracle pass (layout, bf16 dispatch, combine) over the first T_s
+    tokens of the workload; returns (callable, algorithmic bytes)."""
+    import numpy as np
+    import oracle
+    from combine_moe_dispatch_02_gb300.inputs import bf16_bits
+    idx = inp.topk_idx[:T_s].numpy()
+    w = inp.topk_w[:T_s].numpy()
+    xb = bf16_bits(inp.x[:T_s])
+    # y rows for these tokens: the first T_s * K expert-major rows stand in
+    yb = bf16_bits(inp.y[: T_s * wl.K])
+    Lo = oracle.layout(idx, w, wl.E, wl.R)
+    ab = algorithmic_bytes(T_s, wl.H, wl.E, wl.R, wl.K, Lo.n_pairs, int(Lo.expert_offset[wl.E]), Lo.capacity)
+
+    def run():
+        L = oracle.layout(idx, w, wl.E, wl.R)
+        oracle.dispatch_bf16(xb, L)
+        oracle.combine(yb, L.expert_slot, w)
+    return run, ab["layout"] + ab["dispatch"] + ab["combine"]
+
+
+def cpu_baseline(wl, inp, budget_s=10.0):
+    """The oracle as it stands, single-threaded, timed on this host over the
+    full workload repeated until about `budget_s` seconds have passed."""
+    run, nbytes = oracle_step_fn(wl, inp, wl.T)
+    run()  # warm-up
+    t0 = time.perf_counter()
+    n = 0
+    while True:
+        run()
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / n
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"full workload ({wl.T} tokens) x {n} passes of layout + bf16 dispatch + combine, "
+                      f"{dt:.3f} s each, 1 thread", "host_cpu": _cpu_name(), "host_cores": os.cpu_count()}
+
+
+def _cpu_name():
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith(("model name", "cpu part")):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def run_reference(args):
+    """Reference arm: the CPU oracle on bounded per-step samples of the
+    workload (the first T_s tokens, T_s sized so the run stays short)."""
+    from combine_moe_dispatch_02_gb300.inputs import WORKLOADS, make_inputs
+    import oracle
+    oracle.build()
+    wl = WORKLOADS[args.workload]
+    inp = make_inputs(wl, seed=0)
+    probe, _ = oracle_step_fn(wl, inp, 128)
+    t0 = time.perf_counter()
+    probe()
+    per_tok = (time.perf_counter() - t0) / 128
+    target = 60.0 / max(args.steps + args.warmup, 1)         # about a minute in total
+    T_s = int(max(32, min(wl.T, target / max(per_tok, 1e-9))))
+    run, nbytes = oracle_step_fn(wl, inp, T_s)
+    for _ in range(args.warmup):
+        run()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        run()
+        times.append(time.perf_counter() - t0)
+    dt = statistics.mean(times)
+    v = round(nbytes / dt / 1e9, 3)
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": {"workload": f"DeepSeek-V3 shape, first {T_s} of {wl.T} tokens per step",
+                                            "T_sample": T_s, "H": wl.H, "E": wl.E, "R": wl.R, "K": wl.K},
+            "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle", "cores": 1,
+                             "sample": f"{T_s} tokens of the 4096-token workload per step, 1 thread",
+                             "host_cpu": _cpu_name()},
+            "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ---------------------------------------------------------------------- main
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args)))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            from combine_moe_dispatch_02_gb300.inputs import WORKLOADS, make_inputs
+            wl = WORKLOADS[args.workload]
+            res["cpu_baseline"] = cpu_baseline(wl, make_inputs(wl, seed=0))
+        print(json.dumps(res))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,178 @@
+// api.cu -- the C ABI of libmoe_ep.so (declared in include/moe_ep.h): host
+// argument checks, carving of caller memory, kernel launches and status
+// read-back.  No allocation, no synchronisation inside the operator calls.
+#include <climits>
+#include <cstring>
+
+#include "moe_common.cuh"
+
+namespace moe {
+
+int32_t sm_count() {
+    static thread_local int cached_dev = -1;
+    static thread_local int cached = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev != cached_dev) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+        cached = n;
+        cached_dev = dev;
+    }
+    return cached;
+}
+
+}  // namespace moe
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool sizes_ok(int32_t T, int32_t K, int32_t E, int32_t R) {
+    return T >= 0 && K >= 1 && E >= 1 && R >= 1 && E % R == 0;
+}
+
+bool sizes_supported(int32_t K, int32_t E, int32_t R) {
+    return K <= MOE_MAX_TOPK && E <= MOE_MAX_EXPERTS && R <= MOE_MAX_RANKS;
+}
+
+int32_t num_tiles_for(int32_t T, int32_t tile_tokens) {
+    const int32_t n = (T + tile_tokens - 1) / tile_tokens;
+    return n < 1 ? 1 : n;
+}
+
+// Arrays carved from the caller's memory, in this order.
+struct Carve {
+    size_t off = 0;
+    char* base;
+    explicit Carve(void* p) : base(static_cast<char*>(p)) {}
+    template <typename T>
+    T* take(size_t count) {
+        T* p = base ? reinterpret_cast<T*>(base + off) : nullptr;
+        off = moe::align_up(off + sizeof(T) * count, 256);
+        return p;
+    }
+};
+
+size_t carve_layout(moe_layout* L, void* mem, int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity,
+                    int32_t tile_tokens, int32_t num_tiles) {
+    Carve c(mem);
+    moe_layout tmp;
+    moe_layout* o = L ? L : &tmp;
+    o->tokens_per_expert = c.take<int32_t>(E);
+    o->expert_offset = c.take<int32_t>(E + 1);
+    o->tokens_per_rank = c.take<int32_t>(R);
+    o->rank_offset = c.take<int32_t>(R + 1);
+    o->recv_expert_offset = c.take<int32_t>(E + 1);
+    o->recv_slot = c.take<int32_t>(static_cast<size_t>(T) * R);
+    o->expert_slot = c.take<int32_t>(static_cast<size_t>(T) * K);
+    o->recv_src_token = c.take<int32_t>(static_cast<size_t>(capacity));
+    o->expert_src_row = c.take<int32_t>(static_cast<size_t>(T) * K);
+    o->expert_weight = c.take<float>(static_cast<size_t>(T) * K);
+    o->status = c.take<uint32_t>(1);
+    const size_t ws_bytes = moe::layout_workspace_bytes(T, K, E, num_tiles);
+    o->workspace = c.take<char>(ws_bytes);
+    o->workspace_bytes = ws_bytes;
+    (void)tile_tokens;
+    return c.off;
+}
+
+moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+uint64_t timeout_of(const moe_tuning* t) {
+    return (t && t->wait_timeout_ns) ? t->wait_timeout_ns : moe::kDefaultWaitNs;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_layout_bytes(int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity) {
+    if (!sizes_ok(T, K, E, R) || capacity < 0) return 0;
+    const int32_t tt = moe::default_tile_tokens(T, K);
+    return carve_layout(nullptr, nullptr, T, K, E, R, capacity, tt, num_tiles_for(T, tt));
+}
+
+moe_status moe_layout_init(moe_layout* L, int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity,
+                           void* device_mem, size_t bytes) {
+    if (!L || !device_mem) return MOE_ERR_INVALID_ARG;
+    if (!sizes_ok(T, K, E, R)) return MOE_ERR_INVALID_ARG;
+    if (!sizes_supported(K, E, R)) return MOE_ERR_UNSUPPORTED;
+    const int64_t worst = static_cast<int64_t>(T) * (K < R ? K : R);
+    if (capacity < worst || capacity > INT32_MAX) return MOE_ERR_INVALID_ARG;
+    if (static_cast<int64_t>(T) * K > INT32_MAX || static_cast<int64_t>(T) * R > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(device_mem) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (bytes < moe_layout_bytes(T, K, E, R, capacity)) return MOE_ERR_INVALID_ARG;
+    std::memset(L, 0, sizeof(*L));
+    L->T = T; L->K = K; L->E = E; L->R = R;
+    L->capacity = capacity;
+    L->tile_tokens = moe::default_tile_tokens(T, K);
+    L->num_tiles = num_tiles_for(T, L->tile_tokens);
+    carve_layout(L, device_mem, T, K, E, R, capacity, L->tile_tokens, L->num_tiles);
+    return MOE_OK;
+}
+
+moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w, int32_t num_experts,
+                               int32_t num_ranks, moe_layout* L, void* stream, const moe_tuning* tuning) {
+    if (!L || !L->workspace || !L->status) return MOE_ERR_INVALID_ARG;
+    if (num_experts != L->E || num_ranks != L->R) return MOE_ERR_INVALID_ARG;
+    if (L->T > 0 && !topk_idx) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_layout(topk_idx, topk_w, L, static_cast<cudaStream_t>(stream), timeout_of(tuning),
+                                        tuning ? tuning->debug_flags : 0u));
+}
+
+moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int fp8, void* recv_x,
+                        float* recv_scales, void* stream, const moe_tuning* tuning) {
+    if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (L->T > 0 && (!x || !recv_x)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv_x)) return MOE_ERR_INVALID_ARG;
+    if (fp8) {
+        if (hidden % 128 != 0 || !recv_scales || !aligned16(recv_scales)) return MOE_ERR_INVALID_ARG;
+    } else if (recv_scales) {
+        return MOE_ERR_INVALID_ARG;
+    }
+    if (tuning && (tuning->num_channels < 0 || tuning->stages < 0 || tuning->stages > 8)) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch(x, hidden, L, fp8 != 0, recv_x, recv_scales,
+                                          static_cast<cudaStream_t>(stream), tuning ? tuning->num_channels : 0,
+                                          tuning ? tuning->stages : 0, timeout_of(tuning)));
+}
+
+moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w, uint16_t* out,
+                       void* stream, const moe_tuning* tuning) {
+    if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (L->T > 0 && (!y || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+    if (tuning && tuning->num_channels < 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine(y, hidden, L, topk_w, out, static_cast<cudaStream_t>(stream),
+                                         tuning ? tuning->num_channels : 0));
+}
+
+moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* flags_out) {
+    if (!L || !L->status) return MOE_ERR_INVALID_ARG;
+    uint32_t flags = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&flags, L->status, sizeof(flags), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (flags_out) *flags_out = flags;
+    if (flags & MOE_DEVERR_EXPERT_ID) return MOE_ERR_EXPERT_ID;
+    if (flags & MOE_DEVERR_CAPACITY) return MOE_ERR_CAPACITY;
+    if (flags & MOE_DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
+    return MOE_OK;
+}
+
+const char* moe_status_string(moe_status s) {
+    switch (s) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_CAPACITY: return "slot outside the receive / expert buffers";
+        case MOE_ERR_TIMEOUT: return "a bounded device wait ran out";
+        case MOE_ERR_CUDA: return "CUDA runtime error";
+        case MOE_ERR_UNSUPPORTED: return "sizes beyond the supported limits";
+        case MOE_ERR_EXPERT_ID: return "expert id outside [-1, E)";
+    }
+    return "unknown status";
+}
+
+int32_t moe_device_sm_count(void) { return moe::sm_count(); }
+
+}  // extern "C"

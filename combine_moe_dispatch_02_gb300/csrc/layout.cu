@@ -1,0 +1,445 @@
+// layout.cu -- dispatch layout: per-expert / per-rank counts, prefix offsets
+// and token <-> slot maps for MoE dispatch and combine.
+//
+// What is computed follows the problem statement of expert-parallel MoE
+// ("Inside the Nebius + PyTorch DeepSeek V3 recipe", section "Mixture-of-
+// experts and wide expert parallelism": experts partitioned across ranks,
+// tokens dispatched to their top-K experts; Hybrid-EP news article,
+// "Availability and Integration": worst-case preallocated receive buffers).
+// The definitions (orderings, primary expert) are documented in moe_ep.h.
+//
+// Two kernels:
+//  1. layout_scan_kernel: one CTA per tile of tokens.  Tile ids come from an
+//     atomic ticket, so a CTA only ever waits on tiles already claimed by
+//     running CTAs.  Per tile: warp-aggregated, order-preserving ranks of
+//     every (t,k) entry among the entries of its expert (match_any + popc
+//     inside a warp, per-warp histograms in shared memory, an exclusive scan
+//     across warps), then a decoupled look-back over the E-wide count vectors
+//     of earlier tiles (a warp inspects 32 predecessors at a time) to get the
+//     tile's prefix.  The same pass counts "primary" pairs.  Every wait is
+//     bounded; the last tile also writes the count / offset outputs.
+//  2. layout_finalize_kernel: turns per-expert ranks into absolute rows and
+//     writes recv_slot, expert_slot, recv_src_token, expert_src_row,
+//     expert_weight and the tails past the last used row.
+#include "moe_common.cuh"
+
+namespace moe {
+
+namespace {
+
+struct ScanArgs {
+    const int32_t* topk_idx;
+    int32_t T, K, E, m;
+    int32_t tile_tokens, num_tiles;
+    LayoutWs ws;
+    uint32_t* status;
+    // count / offset outputs, written by the last tile
+    int32_t *tokens_per_expert, *expert_offset, *tokens_per_rank, *rank_offset, *recv_expert_offset;
+    int32_t R;
+    uint64_t timeout_ns;
+    uint32_t debug_flags;
+};
+
+// True if entry k of a token (expert e, rank e/m) is the primary entry of its
+// rank: no other valid entry of the token on the same rank has a smaller id,
+// and no earlier entry has the same id.
+__device__ __forceinline__ bool is_primary(const int32_t* row, int K, int k, int e, int m) {
+    const int r = e / m;
+    for (int k2 = 0; k2 < K; ++k2) {
+        if (k2 == k) continue;
+        const int e2 = row[k2];
+        if (e2 >= 0 && e2 / m == r && (e2 < e || (e2 == e && k2 < k))) return false;
+    }
+    return true;
+}
+
+// Wait (bounded) until tile j's flag carries generation `gen`; return its
+// state, or kFlagError if the wait ran out or another CTA aborted the scan.
+__device__ uint32_t wait_tile_flag(const uint32_t* flag, uint32_t gen, const ScanArgs& a, bool* timed_out) {
+    uint64_t t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        const uint32_t v = ld_acquire_gpu(flag);
+        if ((v >> 2) == gen && (v & 3u) != 0) return v & 3u;
+        if (ld_relaxed_gpu(&a.ws.hdr->abort) == gen) return kFlagError;
+        if (it == 0) {
+            t0 = globaltimer_ns();
+        } else if (globaltimer_ns() - t0 > a.timeout_ns) {
+            *timed_out = true;
+            return kFlagError;
+        }
+        __nanosleep(it < 16 ? 20 : 200);
+    }
+}
+
+__global__ void __launch_bounds__(kLayoutThreads)
+layout_scan_kernel(ScanArgs a) {
+    extern __shared__ int32_t smem[];
+    const int twoE = 2 * a.E;
+    int32_t* s_idx = smem;                                // [kMaxTileEntries]
+    int32_t* s_hist = s_idx + kMaxTileEntries;            // [warps][2E]
+    int32_t* s_prefix = s_hist + kLayoutWarps * twoE;     // [2E]
+    int32_t* s_agg = s_prefix + twoE;                     // [2E]
+    __shared__ int s_tile;
+    __shared__ uint32_t s_gen;
+    __shared__ int s_lb_count, s_lb_final;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        s_tile = static_cast<int>(atomicAdd(&a.ws.hdr->ticket, 1u));
+        s_gen = (ld_relaxed_gpu(&a.ws.hdr->epoch) & kGenMask) + 1u;
+    }
+    for (int i = tid; i < kLayoutWarps * twoE; i += kLayoutThreads) s_hist[i] = 0;
+    __syncthreads();
+    const int tile = s_tile;
+    const uint32_t gen = s_gen;
+    if (tile >= a.num_tiles) return;   // cannot happen: one CTA per tile
+    if (tile == 0 && tid == 0) *a.status = 0u;   // status covers this call onwards
+
+    const int t0 = tile * a.tile_tokens;
+    const int nt = min(a.tile_tokens, a.T - t0);
+    const int n = nt * a.K;
+
+    // 1. load the tile's entries; ids outside [-1, E) are flagged and masked
+    bool bad = false;
+    for (int i = tid; i < n; i += kLayoutThreads) {
+        int e = a.topk_idx[static_cast<int64_t>(t0) * a.K + i];
+        if (e < -1 || e >= a.E) { bad = true; e = -1; }
+        s_idx[i] = e;
+    }
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_EXPERT_ID);
+
+    // 2. order-preserving ranks inside the tile, warp by warp over contiguous
+    //    segments of 32-entry chunks
+    const int seg = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
+    int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
+    int32_t* my_hist = s_hist + warp * twoE;
+#pragma unroll
+    for (int c = 0; c < kMaxChunksPerWarp; ++c) {
+        lr_e[c] = -1; lr_p[c] = -1; ent_e[c] = -1;
+        if (c * 32 >= seg) continue;            // warp-uniform
+        const int i = warp * seg + c * 32 + lane;
+        const int e = (i < n) ? s_idx[i] : -1;
+        bool prim = false;
+        if (e >= 0) {
+            const int tl = i / a.K, k = i - tl * a.K;
+            prim = is_primary(s_idx + tl * a.K, a.K, k, e, a.m);
+        }
+        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        const uint32_t pmask = __ballot_sync(0xffffffffu, prim) & peers;
+        const uint32_t lt = lanemask_lt();
+        int base_e = 0, base_p = 0;
+        if (e >= 0) { base_e = my_hist[e]; base_p = my_hist[a.E + e]; }
+        __syncwarp();
+        if (e >= 0 && (peers & lt) == 0) {       // lowest lane of its group updates
+            my_hist[e] = base_e + __popc(peers);
+            my_hist[a.E + e] = base_p + __popc(pmask);
+        }
+        __syncwarp();
+        if (e >= 0) {
+            ent_e[c] = e;
+            lr_e[c] = base_e + __popc(peers & lt);
+            if (prim) lr_p[c] = base_p + __popc(pmask & lt);
+        }
+    }
+    __syncthreads();
+
+    // 3. exclusive scan of the per-warp histograms; tile aggregate
+    for (int col = tid; col < twoE; col += kLayoutThreads) {
+        int run = 0;
+        for (int w = 0; w < kLayoutWarps; ++w) {
+            const int v = s_hist[w * twoE + col];
+            s_hist[w * twoE + col] = run;
+            run += v;
+        }
+        s_agg[col] = run;
+        s_prefix[col] = 0;
+    }
+    __syncthreads();
+
+    // 4. decoupled look-back
+    const bool stall = (a.debug_flags & MOE_DEBUG_STALL_FIRST_TILE) && tile == 0;
+    bool failed = false;
+    if (tile == 0) {
+        for (int col = tid; col < twoE; col += kLayoutThreads) a.ws.tile_incl[col] = s_agg[col];
+        __threadfence();
+        __syncthreads();
+        if (tid == 0 && !stall) st_release_gpu(&a.ws.tile_flag[0], (gen << 2) | kFlagPrefix);
+    } else {
+        int32_t* my_agg = a.ws.tile_agg + static_cast<int64_t>(tile) * twoE;
+        for (int col = tid; col < twoE; col += kLayoutThreads) my_agg[col] = s_agg[col];
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagAgg);
+
+        int hi = tile - 1;                      // nearest tile not yet summed
+        while (true) {
+            if (warp == 0) {
+                const int j = hi - lane;
+                uint32_t st = kFlagPrefix;     // lanes past tile 0 never matter
+                bool timed_out = false;
+                if (j >= 0) st = wait_tile_flag(&a.ws.tile_flag[j], gen, a, &timed_out);
+                const uint32_t err = __ballot_sync(0xffffffffu, j >= 0 && st == kFlagError);
+                const uint32_t pre = __ballot_sync(0xffffffffu, j >= 0 && st == kFlagPrefix);
+                const uint32_t tmo = __ballot_sync(0xffffffffu, timed_out);
+                if (lane == 0) {
+                    if (err) {
+                        s_lb_count = -1;
+                        if (tmo) {
+                            atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_TIMEOUT);
+                            atomicExch(&a.ws.hdr->abort, gen);
+                        }
+                    } else if (pre) {
+                        s_lb_count = __ffs(pre);    // lanes 0..stop inclusive
+                        s_lb_final = 1;
+                    } else {
+                        s_lb_count = min(32, hi + 1);
+                        s_lb_final = 0;
+                    }
+                }
+            }
+            __syncthreads();
+            const int cnt = s_lb_count, fin = s_lb_final;
+            if (cnt < 0) { failed = true; break; }
+            for (int col = tid; col < twoE; col += kLayoutThreads) {
+                int acc = 0;
+                for (int q = 0; q < cnt; ++q) {
+                    const int64_t j = hi - q;
+                    const int32_t* src = (fin && q == cnt - 1) ? a.ws.tile_incl : a.ws.tile_agg;
+                    acc += __ldcg(src + j * twoE + col);
+                }
+                s_prefix[col] += acc;
+            }
+            hi -= cnt;
+            __syncthreads();
+            if (fin) break;
+            if (hi < 0) { failed = true; break; }   // no prefix found: cannot happen
+        }
+        if (failed) {
+            if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagError);
+        } else {
+            int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * twoE;
+            for (int col = tid; col < twoE; col += kLayoutThreads) my_incl[col] = s_prefix[col] + s_agg[col];
+            __threadfence();
+            __syncthreads();
+            if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagPrefix);
+        }
+    }
+    if (failed) return;
+
+    // 5. per-entry ranks including the tile prefix
+#pragma unroll
+    for (int c = 0; c < kMaxChunksPerWarp; ++c) {
+        if (ent_e[c] < 0) continue;
+        const int e = ent_e[c];
+        const int64_t gi = static_cast<int64_t>(t0) * a.K + warp * seg + c * 32 + lane;
+        a.ws.erank[gi] = s_prefix[e] + my_hist[e] + lr_e[c];
+        if (lr_p[c] >= 0) a.ws.prank[gi] = s_prefix[a.E + e] + my_hist[a.E + e] + lr_p[c];
+    }
+
+    // 6. the last tile holds the totals: counts and offsets
+    if (tile == a.num_tiles - 1 && warp == 0) {
+        // s_prefix + s_agg = inclusive totals; exclusive scan over experts
+        for (int half = 0; half < 2; ++half) {
+            int32_t* off = half ? a.recv_expert_offset : a.expert_offset;
+            int carry = 0;
+            for (int base = 0; base < a.E; base += 32) {
+                const int e = base + lane;
+                const int v = (e < a.E) ? s_prefix[half * a.E + e] + s_agg[half * a.E + e] : 0;
+                int incl = v;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const int u = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += u;
+                }
+                if (e < a.E) {
+                    off[e] = carry + incl - v;
+                    if (!half) a.tokens_per_expert[e] = v;
+                }
+                carry += __shfl_sync(0xffffffffu, incl, 31);
+            }
+            if (lane == 0) off[a.E] = carry;
+        }
+    }
+}
+
+// The count / offset outputs written by the last scan tile are read back here
+// (stream order makes them visible).
+struct FinalArgs {
+    const int32_t* topk_idx;
+    const float* topk_w;
+    int32_t T, K, E, R, m;
+    int64_t capacity;
+    LayoutWs ws;
+    uint32_t* status;
+    const int32_t *expert_offset, *recv_expert_offset;
+    int32_t *tokens_per_rank, *rank_offset;
+    int32_t *recv_slot, *expert_slot, *recv_src_token, *expert_src_row;
+    float* expert_weight;
+};
+
+__global__ void __launch_bounds__(256)
+layout_finalize_kernel(FinalArgs a) {
+    extern __shared__ int32_t s_off[];   // [E+1] expert_offset, [E+1] recv_expert_offset
+    int32_t* s_eoff = s_off;
+    int32_t* s_poff = s_off + a.E + 1;
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
+        s_eoff[i] = a.expert_offset[i];
+        s_poff[i] = a.recv_expert_offset[i];
+    }
+    __syncthreads();
+    const int64_t n_entries = static_cast<int64_t>(a.T) * a.K;
+    // clamped: after a failed scan the offsets may be stale
+    const int64_t n_valid = min(max(static_cast<int64_t>(s_eoff[a.E]), int64_t{0}), n_entries);
+    const int64_t n_pairs = min(max(static_cast<int64_t>(s_poff[a.E]), int64_t{0}), a.capacity);
+    const int64_t tid0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    bool bad = false;
+
+    if (blockIdx.x == 0) {
+        for (int r = threadIdx.x; r <= a.R; r += blockDim.x) {
+            a.rank_offset[r] = s_poff[r * a.m];
+            if (r < a.R) a.tokens_per_rank[r] = s_poff[(r + 1) * a.m] - s_poff[r * a.m];
+        }
+        if (threadIdx.x == 0) {
+            // move the scan's error bits into the status word, make the next
+            // call's scan start from a fresh ticket and generation
+            const uint32_t k1 = atomicExch(&a.ws.hdr->k1_err, 0u);
+            if (k1) atomicOr(a.status, k1);
+            a.ws.hdr->ticket = 0u;
+            a.ws.hdr->epoch = (a.ws.hdr->epoch + 1u) % kGenMask;
+        }
+    }
+
+    for (int64_t t = tid0; t < a.T; t += nthreads) {
+        const int32_t* row = a.topk_idx + t * a.K;
+        int32_t* rs_row = a.recv_slot + t * a.R;
+        for (int r = 0; r < a.R; ++r) rs_row[r] = -1;
+        for (int k = 0; k < a.K; ++k) {
+            const int e = row[k];
+            int32_t es = -1;
+            if (e >= 0 && e < a.E) {
+                const int64_t v = static_cast<int64_t>(s_eoff[e]) + a.ws.erank[t * a.K + k];
+                if (v >= 0 && v < n_entries) es = static_cast<int32_t>(v); else bad = true;
+            }
+            a.expert_slot[t * a.K + k] = es;
+        }
+        // receive rows of this token, one per rank that holds one of its experts
+        for (int k = 0; k < a.K; ++k) {
+            const int e = row[k];
+            if (e < 0 || e >= a.E) continue;
+            bool prim = true;
+            for (int k2 = 0; k2 < a.K; ++k2) {
+                const int e2 = row[k2];
+                if (k2 != k && e2 >= 0 && e2 < a.E && e2 / a.m == e / a.m && (e2 < e || (e2 == e && k2 < k))) {
+                    prim = false;
+                    break;
+                }
+            }
+            if (!prim) continue;
+            const int64_t v = static_cast<int64_t>(s_poff[e]) + a.ws.prank[t * a.K + k];
+            if (v >= 0 && v < a.capacity && v < n_pairs) {
+                rs_row[e / a.m] = static_cast<int32_t>(v);
+                a.recv_src_token[v] = static_cast<int32_t>(t);
+            } else {
+                bad = true;
+            }
+        }
+        // expert-major rows point back at the receive row and carry the weight
+        for (int k = 0; k < a.K; ++k) {
+            const int e = row[k];
+            if (e < 0 || e >= a.E) continue;
+            const int32_t es = a.expert_slot[t * a.K + k];
+            if (es < 0) continue;
+            a.expert_src_row[es] = rs_row[e / a.m];
+            a.expert_weight[es] = a.topk_w ? a.topk_w[t * a.K + k] : 0.0f;
+        }
+    }
+    // tails past the last used rows
+    for (int64_t i = n_pairs + tid0; i < a.capacity; i += nthreads) a.recv_src_token[i] = -1;
+    for (int64_t i = n_valid + tid0; i < n_entries; i += nthreads) {
+        a.expert_src_row[i] = -1;
+        a.expert_weight[i] = 0.0f;
+    }
+    if (s_poff[a.E] > a.capacity) bad = true;
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+}
+
+}  // namespace
+
+int32_t default_tile_tokens(int32_t T, int32_t K) {
+    int32_t tt = 1024 / K;                  // about 1024 entries per tile
+    if (tt < 1) tt = 1;
+    if (T > 0 && tt > T) tt = T;
+    return tt;
+}
+
+size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles) {
+    size_t b = sizeof(WsHeader);
+    b = align_up(b + sizeof(uint32_t) * num_tiles, 256);
+    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * 2 * E, 256);
+    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * 2 * E, 256);
+    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
+    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
+    return b;
+}
+
+LayoutWs layout_workspace(const moe_layout* L) {
+    char* p = static_cast<char*>(L->workspace);
+    LayoutWs ws;
+    size_t off = 0;
+    ws.hdr = reinterpret_cast<WsHeader*>(p + off);
+    off += sizeof(WsHeader);
+    ws.tile_flag = reinterpret_cast<uint32_t*>(p + off);
+    off = align_up(off + sizeof(uint32_t) * L->num_tiles, 256);
+    ws.tile_agg = reinterpret_cast<int32_t*>(p + off);
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * 2 * L->E, 256);
+    ws.tile_incl = reinterpret_cast<int32_t*>(p + off);
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * 2 * L->E, 256);
+    ws.erank = reinterpret_cast<int32_t*>(p + off);
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->T) * L->K, 256);
+    ws.prank = reinterpret_cast<int32_t*>(p + off);
+    return ws;
+}
+
+cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const moe_layout* L,
+                          cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags) {
+    const LayoutWs ws = layout_workspace(L);
+    ScanArgs sa;
+    sa.topk_idx = topk_idx;
+    sa.T = L->T; sa.K = L->K; sa.E = L->E; sa.m = L->E / L->R; sa.R = L->R;
+    sa.tile_tokens = L->tile_tokens; sa.num_tiles = L->num_tiles;
+    sa.ws = ws; sa.status = L->status;
+    sa.tokens_per_expert = L->tokens_per_expert; sa.expert_offset = L->expert_offset;
+    sa.tokens_per_rank = L->tokens_per_rank; sa.rank_offset = L->rank_offset;
+    sa.recv_expert_offset = L->recv_expert_offset;
+    sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
+    const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * 2 * static_cast<size_t>(L->E));
+    cudaError_t err = cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem1));
+    if (err != cudaSuccess) return err;
+    layout_scan_kernel<<<L->num_tiles, kLayoutThreads, smem1, stream>>>(sa);
+    err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+
+    FinalArgs fa;
+    fa.topk_idx = topk_idx; fa.topk_w = topk_w;
+    fa.T = L->T; fa.K = L->K; fa.E = L->E; fa.R = L->R; fa.m = L->E / L->R;
+    fa.capacity = L->capacity; fa.ws = ws; fa.status = L->status;
+    fa.expert_offset = L->expert_offset; fa.recv_expert_offset = L->recv_expert_offset;
+    fa.tokens_per_rank = L->tokens_per_rank; fa.rank_offset = L->rank_offset;
+    fa.recv_slot = L->recv_slot; fa.expert_slot = L->expert_slot; fa.recv_src_token = L->recv_src_token;
+    fa.expert_src_row = L->expert_src_row; fa.expert_weight = L->expert_weight;
+    const int threads = 256;
+    int64_t work = L->T;
+    if (L->capacity > work) work = L->capacity;
+    if (static_cast<int64_t>(L->T) * L->K > work) work = static_cast<int64_t>(L->T) * L->K;
+    int64_t blocks = (work + threads - 1) / threads;
+    const int64_t max_blocks = static_cast<int64_t>(sm_count()) * 8;
+    if (blocks > max_blocks) blocks = max_blocks;
+    if (blocks < 1) blocks = 1;
+    const size_t smem2 = sizeof(int32_t) * 2 * (static_cast<size_t>(L->E) + 1);
+    layout_finalize_kernel<<<static_cast<unsigned>(blocks), threads, smem2, stream>>>(fa);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

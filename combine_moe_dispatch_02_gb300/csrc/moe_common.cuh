@@ -1,0 +1,200 @@
+// moe_common.cuh -- device helpers shared by the dispatch-layout, dispatch and
+// combine kernels: inline PTX for mbarriers, TMA bulk copies and memory
+// ordering, bounded waits, and the layout workspace description.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "moe_ep.h"
+
+namespace moe {
+
+constexpr uint64_t kDefaultWaitNs = 1000000000ull;  // 1 s bound on any device wait
+
+// ----------------------------------------------------------------- workspace
+
+// Header at the start of the layout workspace.  `ticket` hands out scan-tile
+// ids in CTA start order; `epoch` numbers layout calls so that progress flags
+// of an earlier call never look current; `k1_err` gathers the scan kernel's
+// error bits until the finalize kernel moves them into the status word;
+// `abort` is set to the current generation once any wait gave up.
+struct WsHeader {
+    uint32_t ticket;
+    uint32_t epoch;
+    uint32_t k1_err;
+    uint32_t abort;
+    uint32_t pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is one 256-byte line");
+
+struct LayoutWs {
+    WsHeader* hdr;
+    uint32_t* tile_flag;   // [num_tiles]: (generation << 2) | state
+    int32_t*  tile_agg;    // [num_tiles][2E]: this tile's counts (expert, primary)
+    int32_t*  tile_incl;   // [num_tiles][2E]: counts of tiles 0..i inclusive
+    int32_t*  erank;       // [T*K]: rank of entry among entries of its expert
+    int32_t*  prank;       // [T*K]: rank of a primary entry among its expert's primaries
+};
+
+enum : uint32_t { kFlagAgg = 1u, kFlagPrefix = 2u, kFlagError = 3u };
+constexpr uint32_t kGenMask = (1u << 30) - 1u;   // generations live in [1, 2^30)
+
+constexpr int kLayoutThreads = 256;
+constexpr int kLayoutWarps = kLayoutThreads / 32;
+constexpr int kMaxTileEntries = 2048;                                   // T_tile * K
+constexpr int kMaxChunksPerWarp = kMaxTileEntries / (kLayoutWarps * 32);  // 8
+
+__host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// ------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t lanemask_lt() {
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
+// mbarrier (CTA scope) ---------------------------------------------------
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(smem_addr(bar)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok) : "r"(smem_addr(bar)), "r"(parity) : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of `bar` to complete, for at most `timeout_ns`.
+// Returns false if the bound ran out.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+    }
+}
+
+// TMA bulk copies (non-tensor) -------------------------------------------
+
+// global -> shared, completion signalled as transaction bytes on `bar`.
+// Both addresses 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* smem_dst, const void* gsrc, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        :: "r"(smem_addr(smem_dst)), "l"(gsrc), "r"(bytes), "r"(smem_addr(bar)) : "memory");
+}
+
+// shared -> global, tracked by this thread's bulk async-groups.
+__device__ __forceinline__ void bulk_s2g(void* gdst, const void* smem_src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 :: "l"(gdst), "r"(smem_addr(smem_src)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until at most N of this thread's bulk groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read %0;" :: "n"(N) : "memory");
+}
+
+// Runtime-count form of bulk_wait_read (the PTX operand is an immediate).
+__device__ __forceinline__ void bulk_wait_read_n(int n) {
+    switch (n) {
+        case 0: bulk_wait_read<0>(); break;
+        case 1: bulk_wait_read<1>(); break;
+        case 2: bulk_wait_read<2>(); break;
+        case 3: bulk_wait_read<3>(); break;
+        case 4: bulk_wait_read<4>(); break;
+        case 5: bulk_wait_read<5>(); break;
+        case 6: bulk_wait_read<6>(); break;
+        default: bulk_wait_read<7>(); break;
+    }
+}
+
+// Wait until all of this thread's bulk groups have completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Order this thread's generic-proxy shared-memory accesses before later
+// async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Streaming 16-byte global accesses --------------------------------------
+
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_stream_v4(uint4* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+}  // namespace moe
+
+// Launch helpers implemented in the per-operator translation units.
+namespace moe {
+cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const moe_layout* L,
+                          cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags);
+cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
+                            void* recv_x, float* recv_scales, cudaStream_t stream,
+                            int32_t num_channels, int32_t stages, uint64_t timeout_ns);
+cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
+                           uint16_t* out, cudaStream_t stream, int32_t num_channels);
+LayoutWs layout_workspace(const moe_layout* L);
+size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles);
+int32_t default_tile_tokens(int32_t T, int32_t K);
+int32_t sm_count();
+}  // namespace moe

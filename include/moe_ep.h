@@ -1,0 +1,179 @@
+/*
+ * moe_ep.h -- C ABI of libmoe_ep.so: MoE token dispatch / combine on one GPU.
+ *
+ * The operators are the dispatch and combine of expert-parallel MoE layers
+ * as Hybrid-EP and DeepEP implement them: dispatch sends every token to the
+ * ranks that hold its top-K experts, combine brings the expert outputs back
+ * to the token's original position ("Inside the Nebius + PyTorch DeepSeek V3
+ * recipe", section "Mixture-of-experts and wide expert parallelism";
+ * Hybrid-EP news article, section "Technical Structure").  Here the EP ranks
+ * are virtual: contiguous blocks of E/R experts whose receive rows live in
+ * one packed buffer in this GPU's HBM, so there is no cross-GPU transport.
+ *
+ * Conventions shared by every call:
+ *  - All tensors are row-major device memory owned by the caller.  The
+ *    library allocates nothing and never synchronises inside the three
+ *    operator calls (moe_dispatch_layout, moe_dispatch, moe_combine).
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Work is enqueued in stream order and the call returns at once.
+ *  - Host-side argument checks return a moe_status synchronously and enqueue
+ *    nothing on failure.  A failed kernel launch returns MOE_ERR_CUDA.
+ *  - Device-side problems (an expert id outside [-1, E), a slot outside the
+ *    buffers, a bounded wait that ran out) never fault: the offending access
+ *    is skipped, a bit is set in the layout's device status word and the
+ *    kernel goes on or returns.  moe_layout_read_status() reports it.
+ *  - bf16 is passed as uint16_t bit patterns; FP8 is OCP E4M3 bytes.
+ *  - Calls that share one moe_layout must be stream-ordered (one stream, or
+ *    events between streams); overlapping calls on one layout race.
+ */
+#ifndef MOE_EP_H
+#define MOE_EP_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,   /* bad size, null or misaligned pointer        */
+    MOE_ERR_CAPACITY = 2,      /* device: a slot fell outside the buffers     */
+    MOE_ERR_TIMEOUT = 3,       /* device: a bounded wait ran out              */
+    MOE_ERR_CUDA = 4,          /* a CUDA runtime call or launch failed        */
+    MOE_ERR_UNSUPPORTED = 5,   /* sizes beyond the documented limits          */
+    MOE_ERR_EXPERT_ID = 6      /* device: an expert id outside [-1, E)        */
+} moe_status;
+
+/* Bits of the device status word (moe_layout.status). */
+#define MOE_DEVERR_EXPERT_ID 0x1u
+#define MOE_DEVERR_CAPACITY  0x2u
+#define MOE_DEVERR_TIMEOUT   0x4u
+
+/* Limits (MOE_ERR_UNSUPPORTED beyond them). */
+#define MOE_MAX_EXPERTS 1024
+#define MOE_MAX_TOPK    32
+#define MOE_MAX_RANKS   256
+
+/* Test hook bits for moe_tuning.debug_flags (0 in production). */
+#define MOE_DEBUG_STALL_FIRST_TILE 0x1u  /* layout: the first scan tile never publishes,
+                                            so its successors' bounded waits run out */
+
+/* Optional launch tuning; pass NULL for the defaults. */
+typedef struct moe_tuning {
+    int32_t  num_channels;     /* CTAs ("independent channels") for dispatch / combine; 0 = auto */
+    int32_t  stages;           /* dispatch pipeline depth per channel; 0 = auto                  */
+    uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                  */
+    uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                         */
+    uint32_t reserved;
+} moe_tuning;
+
+/*
+ * Routing layout.  Notation: T tokens, K top-k, E experts, R virtual ranks,
+ * m = E / R experts per rank, rank(e) = e / m (contiguous expert blocks;
+ * the pages say each GPU holds a subset, e.g. 8 of 256 experts, but not
+ * which one).
+ *
+ *  tokens_per_expert[E]    #{(t,k) : topk_idx[t,k] == e}
+ *  expert_offset[E+1]      exclusive prefix of tokens_per_expert
+ *  tokens_per_rank[R]      #{t : token t has an expert on rank r}
+ *  rank_offset[R+1]        first receive row of each rank; rank_offset[R] = number of pairs
+ *  recv_expert_offset[E+1] exclusive prefix of the per-expert counts of
+ *                          "primary" pairs: the primary expert of (t, r) is
+ *                          the smallest id token t has on rank r
+ *  recv_slot[T,R]          receive row of token t on rank r, or -1.  Rows are
+ *                          ordered by (primary expert, token), so each rank's
+ *                          rows are contiguous and grouped by expert.
+ *  expert_slot[T,K]        expert-major row of entry (t,k), ordered by
+ *                          (expert, token, k); -1 for a masked entry
+ *  recv_src_token[cap]     token of each receive row; -1 past the last pair
+ *  expert_src_row[T*K]     receive row holding each expert-major row's token; -1 past the end
+ *  expert_weight[T*K]      router weight of each expert-major row; 0 past the end
+ *  status                  device status word (MOE_DEVERR_* bits) of the latest
+ *                          moe_dispatch_layout and the calls after it
+ *
+ * The receive buffer is preallocated for the worst case, capacity >=
+ * T * min(K, R) rows (Hybrid-EP news article, "Availability and
+ * Integration": worst-case buffer preallocation for dynamic routing), so no
+ * count has to travel back to the host.
+ */
+typedef struct moe_layout {
+    int32_t T, K, E, R;
+    int64_t capacity;
+    int32_t tile_tokens;        /* tokens per scan tile, fixed at init */
+    int32_t num_tiles;
+    int32_t *tokens_per_expert, *expert_offset, *tokens_per_rank, *rank_offset;
+    int32_t *recv_expert_offset, *recv_slot, *expert_slot, *recv_src_token, *expert_src_row;
+    float   *expert_weight;
+    uint32_t *status;
+    void    *workspace;         /* scan scratch, carved from the same memory */
+    size_t   workspace_bytes;
+} moe_layout;
+
+/* Bytes of device memory moe_layout_init needs for these sizes (outputs +
+ * scan workspace, each array 256-byte aligned).  0 if the sizes are invalid. */
+size_t moe_layout_bytes(int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity);
+
+/* Carve the layout's arrays out of caller memory.  Host only: no CUDA call.
+ * `device_mem` must be 256-byte aligned, hold moe_layout_bytes(...) bytes and
+ * be ZERO-FILLED before its first use (the scan's progress flags start at
+ * zero); afterwards the library keeps it consistent itself.
+ * capacity must be >= T * min(K, R). */
+moe_status moe_layout_init(moe_layout* L, int32_t T, int32_t K, int32_t E, int32_t R,
+                           int64_t capacity, void* device_mem, size_t bytes);
+
+/* Dispatch layout: counts, prefix offsets and token<->slot maps (all fields
+ * above) from topk_idx int32 [T,K] (-1 = masked) and topk_w fp32 [T,K]
+ * (may be NULL: expert_weight is then zero-filled).  Two kernels: a
+ * warp-aggregated per-tile histogram with a decoupled-lookback scan over
+ * E-wide count vectors (tiles claim ids from a ticket so every wait is on a
+ * running CTA; every wait is bounded), then a finalize pass.
+ * num_experts / num_ranks must equal L->E / L->R. */
+moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w,
+                               int32_t num_experts, int32_t num_ranks,
+                               moe_layout* L, void* stream, const moe_tuning* tuning);
+
+/* Dispatch: for every pair with recv_slot[t,r] >= 0 write token t's row into
+ * receive row recv_slot[t,r]: each token once per destination rank, rows in
+ * expert-contiguous order.
+ *   fp8 == 0: recv_x is bf16 [capacity, hidden]; recv_scales must be NULL.
+ *   fp8 != 0: recv_x is E4M3 bytes [capacity, hidden] and recv_scales fp32
+ *     [capacity, hidden/128]: per token and 1x128 block, s = amax / 448 (fp32,
+ *     round to nearest), q = E4M3(x / s) with round-to-nearest-even and
+ *     saturation; an all-zero block gives s = 0 and q = 0.  FP8 dispatch:
+ *     "MoE / Hybrid-EP Validation", "FP8 dispatch restriction"; the pages give
+ *     no recipe, this one is the DeepEP-style 1x128 block scaling.
+ * x is bf16 [T, hidden]; hidden % 8 == 0 (hidden % 128 == 0 for fp8); x,
+ * recv_x, recv_scales 16-byte aligned.  Rows past rank_offset[R] are not
+ * written.  Each CTA is an independent channel over a contiguous chunk of
+ * tokens: TMA bulk loads of the row into shared memory, then one TMA bulk
+ * store per destination row; no grid-wide synchronisation (Hybrid-EP news
+ * article, "Technical Structure": each CUDA block an independent channel). */
+moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int fp8,
+                        void* recv_x, float* recv_scales, void* stream, const moe_tuning* tuning);
+
+/* Combine: out[t,:] = bf16_rne( sum over k = 0..K-1 with expert_slot[t,k] >= 0
+ * of topk_w[t,k] * y[expert_slot[t,k], :] ), accumulated in fp32 as a fused
+ * multiply-add chain starting from 0 in ascending k.  y is bf16 [T*K, hidden]
+ * in expert-major row order (row expert_offset[e] + j is expert e's j-th
+ * entry); out is bf16 [T, hidden]; a token with every entry masked gets +0.
+ * hidden % 8 == 0; y and out 16-byte aligned. */
+moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L,
+                       const float* topk_w, uint16_t* out, void* stream, const moe_tuning* tuning);
+
+/* Synchronise `stream`, read the device status word, and map it to a status
+ * (expert-id errors first, then capacity, then timeout).  `flags_out` (may be
+ * NULL) receives the raw MOE_DEVERR_* bits. */
+moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* flags_out);
+
+/* Human-readable name of a status code (static storage). */
+const char* moe_status_string(moe_status s);
+
+/* Number of SMs of the current device (0 on error); used for channel counts. */
+int32_t moe_device_sm_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MOE_EP_H */

@@ -1,0 +1,80 @@
+"""The C-ABI library builds, loads and exports every function declared in
+include/moe_ep.h; host-only entry points validate their arguments.  No
+GPU and no compute call: the calls below return before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_moe_dispatch_02_gb300 import build, ep
+    build.build()
+    return ep.lib()
+
+
+def _declared_functions():
+    src = open(os.path.join(ROOT, "include", "moe_ep.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_0-9]+)\s*\(", src)))
+
+
+def test_header_declares_the_operator_calls():
+    names = _declared_functions()
+    for n in ("moe_dispatch_layout", "moe_dispatch", "moe_combine", "moe_layout_init", "moe_layout_bytes",
+              "moe_layout_read_status", "moe_status_string"):
+        assert n in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for n in _declared_functions():
+        assert hasattr(lib, n), n
+
+
+def test_binding_names_match_header(lib):
+    from combine_moe_dispatch_02_gb300 import ep
+    assert sorted(ep.EXPORTED) == _declared_functions()
+
+
+def test_layout_bytes_and_init_validation(lib):
+    from combine_moe_dispatch_02_gb300 import ep
+    n = ep.moe_layout_bytes(4096, 8, 256, 8, 4096 * 8)
+    assert n > 4 * (4096 * 8 * 4)           # holds at least recv_slot + expert_slot + ...
+    assert ep.moe_layout_bytes(16, 2, 6, 4, 32) == 0            # E % R != 0
+    L = ep.moe_layout()
+    fake = ctypes.c_void_p(1 << 20)                               # never dereferenced on the host
+    init = lib.moe_layout_init
+    assert init(ctypes.byref(L), 16, 2, 8, 4, 32, fake, n) == ep.MOE_OK
+    assert L.T == 16 and L.num_tiles >= 1 and L.capacity == 32
+    assert init(ctypes.byref(L), 16, 2, 8, 4, 31, fake, n) == ep.MOE_ERR_INVALID_ARG         # capacity < T*min(K,R)
+    assert init(ctypes.byref(L), 16, 2, 8, 4, 32, ctypes.c_void_p((1 << 20) + 16), n) == ep.MOE_ERR_INVALID_ARG
+    assert init(ctypes.byref(L), 16, 2, 8, 4, 32, fake, 10) == ep.MOE_ERR_INVALID_ARG        # too small
+    assert init(ctypes.byref(L), 16, 33, 64, 4, 16 * 4, fake, 1 << 30) == ep.MOE_ERR_UNSUPPORTED  # K > 32
+    assert init(ctypes.byref(L), 16, 2, 2048, 4, 32, fake, 1 << 30) == ep.MOE_ERR_UNSUPPORTED    # E > 1024
+
+
+def test_operator_calls_reject_bad_arguments_on_the_host(lib):
+    from combine_moe_dispatch_02_gb300 import ep
+    L = ep.moe_layout()
+    n = ep.moe_layout_bytes(16, 2, 8, 4, 32)
+    assert lib.moe_layout_init(ctypes.byref(L), 16, 2, 8, 4, 32, ctypes.c_void_p(1 << 20), n) == ep.MOE_OK
+    p = ctypes.c_void_p(1 << 21)
+    # expert / rank counts that do not match the layout
+    assert lib.moe_dispatch_layout(p, p, 16, 4, ctypes.byref(L), None, None) == ep.MOE_ERR_INVALID_ARG
+    # hidden not a multiple of 8; misaligned rows; fp8 with hidden % 128 != 0
+    assert lib.moe_dispatch(p, 12, ctypes.byref(L), 0, p, None, None, None) == ep.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(ctypes.c_void_p((1 << 21) + 2), 64, ctypes.byref(L), 0, p, None, None, None) \
+        == ep.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(p, 64, ctypes.byref(L), 1, p, p, None, None) == ep.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(p, 12, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
+    assert lib.moe_combine(None, 64, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
+
+
+def test_status_strings(lib):
+    from combine_moe_dispatch_02_gb300 import ep
+    for s in range(7):
+        assert ep.moe_status_string(s) and ep.moe_status_string(s) != "unknown status"

@@ -1,0 +1,161 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Layout, indices, bf16 rows, FP8 bytes and scales
+must match bit for bit; combine within 1 bf16 ulp (and in practice bit for
+bit: both sides run the same fp32 fma chain in ascending k)."""
+import numpy as np
+import pytest
+import torch
+
+from combine_moe_dispatch_02_gb300.inputs import WORKLOADS, make_inputs, random_routing, random_weights
+from harness import assert_parity, bf16_ulp_diff, gpu_run, oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    from combine_moe_dispatch_02_gb300 import build, ep
+    build.build()
+    ep.lib()
+    import oracle
+    oracle.build()
+
+
+@pytest.mark.parametrize("name", ["tiny", "dsv3", "dsv3_fp8", "qwen_skew", "ds16_wide"])
+def test_workload_parity_full_size(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl)
+    g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8)
+    o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8)
+    assert g["status"] == 0 and o["status"] == 0
+    assert_parity(g, o, fp8=wl.fp8)
+    # combine is bit-exact in practice (same fma chain)
+    assert np.array_equal(g["out"], o["out"])
+
+
+@pytest.mark.parametrize("T,H,E,R,K,mask,dups,fp8,seed", [
+    (1, 8, 1, 1, 1, 0.0, False, False, 0),          # smallest everything
+    (1, 128, 4, 2, 2, 0.0, False, True, 1),
+    (777, 136, 16, 4, 3, 0.1, False, False, 2),      # ragged tokens, odd-ish hidden
+    (1000, 256, 32, 8, 6, 0.2, True, False, 3),      # masked + duplicate ids
+    (1000, 384, 32, 8, 6, 0.2, True, True, 4),       # same for FP8
+    (513, 64, 8, 8, 8, 0.0, False, False, 5),        # one expert per rank, every expert
+    (600, 64, 12, 1, 5, 0.0, False, False, 6),       # a single rank
+    (300, 96, 64, 4, 16, 0.05, False, False, 7),     # top-16: generic combine path
+    (200, 8200, 16, 4, 4, 0.0, False, False, 8),     # rows split into two column chunks
+    (128, 9216, 16, 4, 4, 0.0, False, True, 9),      # FP8 rows split into chunks
+    (2500, 128, 256, 32, 8, 0.0, False, False, 10),  # many tiles, wide ranks
+    (4096, 64, 1024, 256, 32, 0.0, False, False, 11),  # the documented maxima of E, R and K
+])
+def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed):
+    idx = random_routing(T, K, E, seed, mask_frac=mask, allow_duplicates=dups)
+    w = random_weights(T, K, seed)
+    g_ = torch.Generator().manual_seed(seed + 1)
+    x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
+    y = torch.randn(T * K, H, generator=g_).to(torch.bfloat16)
+    g = gpu_run(x, idx, w, y, E, R, fp8=fp8)
+    o = oracle_run(x, idx, w, y, E, R, fp8=fp8)
+    assert g["status"] == 0 and o["status"] == 0
+    assert_parity(g, o, fp8=fp8)
+
+
+def test_zero_tokens():
+    E, R, K, H = 8, 2, 2, 64
+    idx = torch.zeros(0, K, dtype=torch.int32)
+    w = torch.zeros(0, K)
+    x = torch.zeros(0, H, dtype=torch.bfloat16)
+    y = torch.zeros(0, H, dtype=torch.bfloat16)
+    g = gpu_run(x, idx, w, y, E, R)
+    assert g["status"] == 0
+    assert np.all(g["tokens_per_expert"] == 0) and np.all(g["expert_offset"] == 0)
+    assert np.all(g["rank_offset"] == 0) and g["n_pairs"] == 0
+
+
+def test_all_entries_masked():
+    T, E, R, K, H = 100, 8, 4, 3, 32
+    idx = torch.full((T, K), -1, dtype=torch.int32)
+    w = random_weights(T, K, 3)
+    x = torch.randn(T, H).to(torch.bfloat16)
+    y = torch.randn(T * K, H).to(torch.bfloat16)
+    g = gpu_run(x, idx, w, y, E, R)
+    o = oracle_run(x, idx, w, y, E, R)
+    assert_parity(g, o)
+    assert np.all(g["out"] == 0)                     # every token sums nothing: +0
+
+
+def test_fp8_special_blocks():
+    """All-zero blocks, signed zeros, a block whose max sits in one element,
+    large and tiny magnitudes."""
+    T, H, E, R, K = 64, 512, 8, 4, 2
+    idx = random_routing(T, K, E, 5)
+    x = torch.randn(T, H)
+    x[0] = 0.0
+    x[1, :128] = -0.0
+    x[2, 128:256] = 0.0
+    x[2, 200] = -3.0
+    x[3] *= 1e4
+    x[4] *= 1e-30
+    x[5, 256:384] = torch.tensor([1e-38] * 127 + [1.0])
+    x = x.to(torch.bfloat16)
+    g = gpu_run(x, idx, None, None, E, R, fp8=True)
+    o = oracle_run(x, idx, None, None, E, R, fp8=True)
+    assert_parity(g, o, fp8=True)
+
+
+def test_repeated_calls_reuse_workspace():
+    """Several layout calls on one workspace (ticket and generation reuse) give
+    identical results, also when routings alternate."""
+    wl = WORKLOADS["tiny"]
+    a = make_inputs(wl, seed=0)
+    b = make_inputs(wl, seed=1)
+    from combine_moe_dispatch_02_gb300 import ep
+    L = ep.Layout(wl.T, wl.K, wl.E, wl.R)
+    for inp in (a, b, a, b, a):
+        ep.moe_dispatch_layout(inp.topk_idx.cuda(), inp.topk_w.cuda(), wl.E, wl.R, L)
+        assert ep.moe_layout_read_status(L) == (0, 0)
+        o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R)
+        assert np.array_equal(L.recv_slot.cpu().numpy(), o["recv_slot"])
+        assert np.array_equal(L.expert_slot.cpu().numpy(), o["expert_slot"])
+
+
+def test_dispatch_identity_combine_roundtrip_on_gpu():
+    """bf16 dispatch -> identity expert (y row = its receive row) -> combine
+    with renormalised weights returns x exactly."""
+    wl = WORKLOADS["dsv3"]
+    inp = make_inputs(wl, with_y=False)
+    from combine_moe_dispatch_02_gb300 import ep
+    L = ep.Layout(wl.T, wl.K, wl.E, wl.R)
+    x = inp.x.cuda()
+    w = inp.topk_w.cuda()
+    ep.moe_dispatch_layout(inp.topk_idx.cuda(), w, wl.E, wl.R, L)
+    recv, _ = ep.alloc_recv(L, wl.H, False)
+    ep.moe_dispatch(x, L, False, recv)
+    y = recv[L.expert_src_row.long()].contiguous()      # test-only identity expert
+    out = torch.empty_like(x)
+    ep.moe_combine(y, L, w, out)
+    assert ep.moe_layout_read_status(L) == (0, 0)
+    assert torch.equal(out.view(torch.int16), x.view(torch.int16))
+
+
+def test_tuning_variants_agree():
+    """Channel counts and stage depths change scheduling only, not results."""
+    wl = WORKLOADS["dsv3"].scaled(512)
+    inp = make_inputs(wl)
+    o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R)
+    for ch, st in [(1, 2), (4, 3), (16, 8), (1000, 0)]:
+        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, num_channels=ch, stages=st)
+        assert_parity(g, o)
+    o8 = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True)
+    for ch, st in [(1, 2), (7, 4)]:
+        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True, num_channels=ch, stages=st)
+        assert_parity(g, o8, fp8=True)
+
+
+def test_over_provisioned_capacity():
+    wl = WORKLOADS["tiny"]
+    inp = make_inputs(wl)
+    cap = wl.capacity + 333
+    g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, capacity=cap)
+    o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, capacity=cap)
+    assert_parity(g, o)
