@@ -154,9 +154,11 @@ moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* f
     if (cudaMemcpyAsync(&flags, L->status, sizeof(flags), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
     if (flags_out) *flags_out = flags;
+    // a timed-out scan leaves stale ranks behind, which the later kernels
+    // then flag as capacity errors: report the root cause first
+    if (flags & MOE_DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
     if (flags & MOE_DEVERR_EXPERT_ID) return MOE_ERR_EXPERT_ID;
     if (flags & MOE_DEVERR_CAPACITY) return MOE_ERR_CAPACITY;
-    if (flags & MOE_DEVERR_TIMEOUT) return MOE_ERR_TIMEOUT;
     return MOE_OK;
 }
 

@@ -163,8 +163,9 @@ moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L,
                        const float* topk_w, uint16_t* out, void* stream, const moe_tuning* tuning);
 
 /* Synchronise `stream`, read the device status word, and map it to a status
- * (expert-id errors first, then capacity, then timeout).  `flags_out` (may be
- * NULL) receives the raw MOE_DEVERR_* bits. */
+ * (timeout first -- a timed-out scan also makes later kernels see slots out
+ * of range -- then expert ids, then capacity).  `flags_out` (may be NULL)
+ * receives the raw MOE_DEVERR_* bits. */
 moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* flags_out);
 
 /* Human-readable name of a status code (static storage). */
