@@ -21,8 +21,7 @@
 //     output stage, which TMA bulk stores send to every destination row; the
 //     scales go out with plain stores.
 // x is read from HBM once; the receive rows are written once each.
-#include <cuda_fp8.h>
-
+#include "fp8_quant.cuh"
 #include "moe_common.cuh"
 
 namespace moe {
@@ -31,7 +30,7 @@ namespace {
 
 constexpr int kMaxStages = 8;
 constexpr int kSlotBatchInts = 2048;     // recv_slot entries staged per batch
-constexpr int kFp8Threads = 128;
+constexpr int kFp8Threads = 256;
 
 struct DispatchArgs {
     const uint8_t* x;            // bf16 [T, H]
@@ -152,18 +151,9 @@ dispatch_bf16_kernel(DispatchArgs a) {
 
 // FP8 E4M3 ------------------------------------------------------------------
 
-__device__ __forceinline__ uint32_t quantize4(uint2 raw, float s, bool zero_block) {
-    // four bf16 values -> four E4M3 bytes (element 0 in the lowest byte)
-    if (zero_block) return 0u;
-    const float v0 = __uint_as_float(raw.x << 16), v1 = __uint_as_float(raw.x & 0xffff0000u);
-    const float v2 = __uint_as_float(raw.y << 16), v3 = __uint_as_float(raw.y & 0xffff0000u);
-    const __nv_fp8x2_storage_t lo =
-        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(v0, s), __fdiv_rn(v1, s)), __NV_SATFINITE, __NV_E4M3);
-    const __nv_fp8x2_storage_t hi =
-        __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(v2, s), __fdiv_rn(v3, s)), __NV_SATFINITE, __NV_E4M3);
-    return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
-}
-
+// One item = one column chunk of one token.  A 128-column block is 256 bytes of
+// bf16: sixteen lanes hold 16 bytes each, so a warp quantises two blocks at a
+// time; the block amax is reduced across the half-warp.
 __global__ void __launch_bounds__(kFp8Threads)
 dispatch_fp8_kernel(DispatchArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -174,6 +164,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
     uint8_t* rest;
     smem_carve(smem, a, &bars, &s_slots, &rest);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    constexpr int kWarps = kFp8Threads / 32;
     const int S = a.stages;
     const int nbc = a.chunk_elems / 128;                   // blocks per chunk
     const int nb_row = a.H / 128;
@@ -226,26 +217,30 @@ dispatch_fp8_kernel(DispatchArgs a) {
         const bool ok = mbar_wait_bounded(&bars[s], static_cast<uint32_t>(k / S) & 1u, a.timeout_ns);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
 
-        // quantise: warp w takes blocks w, w+4, ...; lane holds 4 consecutive values
+        // quantise: each half-warp takes one 128-column block per pass
         const uint8_t* in = stage_in + static_cast<size_t>(s) * in_bytes;
         uint8_t* out = stage_out + static_cast<size_t>(s) * out_bytes;
-        for (int b = warp; b < nb; b += kFp8Threads / 32) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(in + (b * 128 + lane * 4) * 2);
-            float amax = fmaxf(fmaxf(fabsf(__uint_as_float(raw.x << 16)), fabsf(__uint_as_float(raw.x & 0xffff0000u))),
-                               fmaxf(fabsf(__uint_as_float(raw.y << 16)), fabsf(__uint_as_float(raw.y & 0xffff0000u))));
+        const int hl = lane & 15;
+        for (int base = warp * 2; base < nb; base += 2 * kWarps) {
+            const int b = base + (lane >> 4);
+            const bool active = b < nb;
+            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
+            if (active) raw = *reinterpret_cast<const uint4*>(in + b * 256 + hl * 16);
+            float amax = absmax8(raw);
 #pragma unroll
-            for (int d = 16; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
+            for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
             const float sc = __fdiv_rn(amax, 448.0f);
-            *reinterpret_cast<uint32_t*>(out + b * 128 + lane * 4) = quantize4(raw, sc, amax == 0.0f);
-            if (lane == 0) s_scale[s * nbc + b] = sc;
+            const bool fast = scale_is_normal(sc);
+            const float rc = fast ? __frcp_rn(sc) : 0.0f;
+            if (active) {
+                *reinterpret_cast<uint2*>(out + b * 128 + hl * 8) = quantize8(raw, sc, rc, fast, amax == 0.0f);
+                if (hl == 0) s_scale[s * nbc + b] = sc;
+            }
         }
         fence_proxy_async_smem();
         __syncthreads();
         // the input stage is free again: fetch item k+S into it
-        if (tid == 0 && k + S < rg.n) {
-            fence_proxy_async_smem();
-            issue_load(k + S);
-        }
+        if (tid == 0 && k + S < rg.n) issue_load(k + S);
         const int32_t* trow = s_slots + (t - batch_t0) * a.R;
         if (warp == 0) {
             for (int r = lane; r < a.R; r += 32) {
@@ -273,7 +268,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
 
 cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
                             void* recv_x, float* recv_scales, cudaStream_t stream,
-                            int32_t num_channels, int32_t stages, uint64_t timeout_ns) {
+                            int32_t num_channels, int32_t stages, int32_t chunk_bytes, uint64_t timeout_ns) {
     if (L->T == 0) return cudaSuccess;
     DispatchArgs a;
     a.x = reinterpret_cast<const uint8_t*>(x);
@@ -284,11 +279,12 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     a.capacity = L->capacity;
     a.status = L->status;
     a.timeout_ns = timeout_ns;
-    // column chunks: at most 16 KB of bf16 input per stage
-    const int32_t max_elems = 8192;
+    // column chunks: at most chunk_bytes (default 16 KB) of bf16 input per stage
+    const int32_t max_elems = (chunk_bytes > 0 ? chunk_bytes : 16384) / 2;
     const int32_t gran = fp8 ? 128 : 8;
     a.nchunk = (hidden + max_elems - 1) / max_elems;
     a.chunk_elems = ((hidden + a.nchunk - 1) / a.nchunk + gran - 1) / gran * gran;
+    a.nchunk = (hidden + a.chunk_elems - 1) / a.chunk_elems;   // every chunk non-empty
     a.slot_batch = kSlotBatchInts / L->R;
     if (a.slot_batch < 1) a.slot_batch = 1;
     int S = stages > 0 ? stages : (fp8 ? 3 : 4);

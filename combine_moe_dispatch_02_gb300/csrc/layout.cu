@@ -9,18 +9,21 @@
 // The definitions (orderings, primary expert) are documented in moe_ep.h.
 //
 // Two kernels:
-//  1. layout_scan_kernel: one CTA per tile of tokens.  Tile ids come from an
-//     atomic ticket, so a CTA only ever waits on tiles already claimed by
-//     running CTAs.  Per tile: warp-aggregated, order-preserving ranks of
-//     every (t,k) entry among the entries of its expert (match_any + popc
+//  1. layout_scan_kernel: one CTA per tile of about 2048 (t,k) entries.  Tile
+//     ids come from an atomic ticket, so a CTA only ever waits on tiles that
+//     running CTAs have claimed.  Per tile: warp-aggregated, order-preserving
+//     ranks of every entry among the entries of its expert (match_any + popc
 //     inside a warp, per-warp histograms in shared memory, an exclusive scan
-//     across warps), then a decoupled look-back over the E-wide count vectors
-//     of earlier tiles (a warp inspects 32 predecessors at a time) to get the
-//     tile's prefix.  The same pass counts "primary" pairs.  Every wait is
-//     bounded; the last tile also writes the count / offset outputs.
-//  2. layout_finalize_kernel: turns per-expert ranks into absolute rows and
-//     writes recv_slot, expert_slot, recv_src_token, expert_src_row,
-//     expert_weight and the tails past the last used row.
+//     across warps) and, in the same pass, among the "primary" entries; then
+//     a decoupled look-back over the 2E-wide count vectors of earlier tiles
+//     (one warp inspects 32 predecessors at a time; the vectors are summed
+//     with many loads in flight per thread) gives the tile's prefix.  Every
+//     wait is bounded.  The last tile also writes the count / offset outputs.
+//  2. layout_finalize_kernel: one block per 32 tokens stages the tokens'
+//     entries and ranks in shared memory, adds the expert offsets and writes
+//     recv_slot, expert_slot, recv_src_token, expert_src_row and
+//     expert_weight with coalesced row writes, plus the tails past the last
+//     used row.
 #include "moe_common.cuh"
 
 namespace moe {
@@ -29,13 +32,12 @@ namespace {
 
 struct ScanArgs {
     const int32_t* topk_idx;
-    int32_t T, K, E, m;
+    int32_t T, K, E, m, R;
     int32_t tile_tokens, num_tiles;
     LayoutWs ws;
     uint32_t* status;
     // count / offset outputs, written by the last tile
-    int32_t *tokens_per_expert, *expert_offset, *tokens_per_rank, *rank_offset, *recv_expert_offset;
-    int32_t R;
+    int32_t *tokens_per_expert, *expert_offset, *recv_expert_offset;
     uint64_t timeout_ns;
     uint32_t debug_flags;
 };
@@ -53,25 +55,27 @@ __device__ __forceinline__ bool is_primary(const int32_t* row, int K, int k, int
     return true;
 }
 
-// Wait (bounded) until tile j's flag carries generation `gen`; return its
-// state, or kFlagError if the wait ran out or another CTA aborted the scan.
-__device__ uint32_t wait_tile_flag(const uint32_t* flag, uint32_t gen, const ScanArgs& a, bool* timed_out) {
+constexpr uint32_t kWaitTimedOut = 4u;
+
+// Wait (bounded) until a tile flag carries generation `gen`; return its state,
+// kFlagError if another CTA aborted the scan, or kWaitTimedOut.
+__device__ uint32_t wait_tile_flag(const uint32_t* flag, uint32_t gen, const uint32_t* abort_word,
+                                   uint64_t timeout_ns) {
     uint64_t t0 = 0;
     for (uint32_t it = 0;; ++it) {
         const uint32_t v = ld_acquire_gpu(flag);
         if ((v >> 2) == gen && (v & 3u) != 0) return v & 3u;
-        if (ld_relaxed_gpu(&a.ws.hdr->abort) == gen) return kFlagError;
+        if (ld_relaxed_gpu(abort_word) == gen) return kFlagError;
         if (it == 0) {
             t0 = globaltimer_ns();
-        } else if (globaltimer_ns() - t0 > a.timeout_ns) {
-            *timed_out = true;
-            return kFlagError;
+        } else if (globaltimer_ns() - t0 > timeout_ns) {
+            return kWaitTimedOut;
         }
-        __nanosleep(it < 16 ? 20 : 200);
+        __nanosleep(it < 32 ? 32 : 256);
     }
 }
 
-__global__ void __launch_bounds__(kLayoutThreads)
+__global__ void __launch_bounds__(kLayoutThreads, 1)
 layout_scan_kernel(ScanArgs a) {
     extern __shared__ int32_t smem[];
     const int twoE = 2 * a.E;
@@ -93,13 +97,13 @@ layout_scan_kernel(ScanArgs a) {
     const int tile = s_tile;
     const uint32_t gen = s_gen;
     if (tile >= a.num_tiles) return;   // cannot happen: one CTA per tile
-    if (tile == 0 && tid == 0) *a.status = 0u;   // status covers this call onwards
+    if (tile == 0 && tid == 0) *a.status = 0u;   // the status word covers this call onwards
 
     const int t0 = tile * a.tile_tokens;
     const int nt = min(a.tile_tokens, a.T - t0);
     const int n = nt * a.K;
 
-    // 1. load the tile's entries; ids outside [-1, E) are flagged and masked
+    // 1. the tile's entries; ids outside [-1, E) are flagged and masked
     bool bad = false;
     for (int i = tid; i < n; i += kLayoutThreads) {
         int e = a.topk_idx[static_cast<int64_t>(t0) * a.K + i];
@@ -108,8 +112,8 @@ layout_scan_kernel(ScanArgs a) {
     }
     if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_EXPERT_ID);
 
-    // 2. order-preserving ranks inside the tile, warp by warp over contiguous
-    //    segments of 32-entry chunks
+    // 2. order-preserving ranks inside the tile: warp w owns a contiguous
+    //    segment of 32-entry chunks and keeps its own histogram
     const int seg = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
     int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
     int32_t* my_hist = s_hist + warp * twoE;
@@ -146,6 +150,7 @@ layout_scan_kernel(ScanArgs a) {
     // 3. exclusive scan of the per-warp histograms; tile aggregate
     for (int col = tid; col < twoE; col += kLayoutThreads) {
         int run = 0;
+#pragma unroll
         for (int w = 0; w < kLayoutWarps; ++w) {
             const int v = s_hist[w * twoE + col];
             s_hist[w * twoE + col] = run;
@@ -176,11 +181,10 @@ layout_scan_kernel(ScanArgs a) {
             if (warp == 0) {
                 const int j = hi - lane;
                 uint32_t st = kFlagPrefix;     // lanes past tile 0 never matter
-                bool timed_out = false;
-                if (j >= 0) st = wait_tile_flag(&a.ws.tile_flag[j], gen, a, &timed_out);
-                const uint32_t err = __ballot_sync(0xffffffffu, j >= 0 && st == kFlagError);
+                if (j >= 0) st = wait_tile_flag(&a.ws.tile_flag[j], gen, &a.ws.hdr->abort, a.timeout_ns);
+                const uint32_t err = __ballot_sync(0xffffffffu, j >= 0 && (st == kFlagError || st == kWaitTimedOut));
                 const uint32_t pre = __ballot_sync(0xffffffffu, j >= 0 && st == kFlagPrefix);
-                const uint32_t tmo = __ballot_sync(0xffffffffu, timed_out);
+                const uint32_t tmo = __ballot_sync(0xffffffffu, st == kWaitTimedOut);
                 if (lane == 0) {
                     if (err) {
                         s_lb_count = -1;
@@ -189,7 +193,7 @@ layout_scan_kernel(ScanArgs a) {
                             atomicExch(&a.ws.hdr->abort, gen);
                         }
                     } else if (pre) {
-                        s_lb_count = __ffs(pre);    // lanes 0..stop inclusive
+                        s_lb_count = __ffs(pre);    // lanes 0..nearest prefix tile
                         s_lb_final = 1;
                     } else {
                         s_lb_count = min(32, hi + 1);
@@ -200,8 +204,11 @@ layout_scan_kernel(ScanArgs a) {
             __syncthreads();
             const int cnt = s_lb_count, fin = s_lb_final;
             if (cnt < 0) { failed = true; break; }
+            // sum the window's vectors: independent L2 loads, unrolled so that
+            // several are in flight per thread
             for (int col = tid; col < twoE; col += kLayoutThreads) {
                 int acc = 0;
+#pragma unroll 8
                 for (int q = 0; q < cnt; ++q) {
                     const int64_t j = hi - q;
                     const int32_t* src = (fin && q == cnt - 1) ? a.ws.tile_incl : a.ws.tile_agg;
@@ -236,29 +243,27 @@ layout_scan_kernel(ScanArgs a) {
         if (lr_p[c] >= 0) a.ws.prank[gi] = s_prefix[a.E + e] + my_hist[a.E + e] + lr_p[c];
     }
 
-    // 6. the last tile holds the totals: counts and offsets
-    if (tile == a.num_tiles - 1 && warp == 0) {
-        // s_prefix + s_agg = inclusive totals; exclusive scan over experts
-        for (int half = 0; half < 2; ++half) {
-            int32_t* off = half ? a.recv_expert_offset : a.expert_offset;
-            int carry = 0;
-            for (int base = 0; base < a.E; base += 32) {
-                const int e = base + lane;
-                const int v = (e < a.E) ? s_prefix[half * a.E + e] + s_agg[half * a.E + e] : 0;
-                int incl = v;
+    // 6. the last tile holds the totals: counts and offsets (warp w < 2 scans half w)
+    if (tile == a.num_tiles - 1 && warp < 2) {
+        const int half = warp;
+        int32_t* off = half ? a.recv_expert_offset : a.expert_offset;
+        int carry = 0;
+        for (int base = 0; base < a.E; base += 32) {
+            const int e = base + lane;
+            const int v = (e < a.E) ? s_prefix[half * a.E + e] + s_agg[half * a.E + e] : 0;
+            int incl = v;
 #pragma unroll
-                for (int d = 1; d < 32; d <<= 1) {
-                    const int u = __shfl_up_sync(0xffffffffu, incl, d);
-                    if (lane >= d) incl += u;
-                }
-                if (e < a.E) {
-                    off[e] = carry + incl - v;
-                    if (!half) a.tokens_per_expert[e] = v;
-                }
-                carry += __shfl_sync(0xffffffffu, incl, 31);
+            for (int d = 1; d < 32; d <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, incl, d);
+                if (lane >= d) incl += u;
             }
-            if (lane == 0) off[a.E] = carry;
+            if (e < a.E) {
+                off[e] = carry + incl - v;
+                if (!half) a.tokens_per_expert[e] = v;
+            }
+            carry += __shfl_sync(0xffffffffu, incl, 31);
         }
+        if (lane == 0) off[a.E] = carry;
     }
 }
 
@@ -277,97 +282,104 @@ struct FinalArgs {
     float* expert_weight;
 };
 
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(kFinalizeThreads)
 layout_finalize_kernel(FinalArgs a) {
-    extern __shared__ int32_t s_off[];   // [E+1] expert_offset, [E+1] recv_expert_offset
-    int32_t* s_eoff = s_off;
-    int32_t* s_poff = s_off + a.E + 1;
-    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) {
+    extern __shared__ int32_t sm[];
+    const int E1 = a.E + 1;
+    int32_t* s_eoff = sm;                                    // [E+1]
+    int32_t* s_poff = s_eoff + E1;                           // [E+1]
+    int32_t* s_idx = s_poff + E1;                            // [TB*K]
+    int32_t* s_er = s_idx + kFinalizeTokens * a.K;           // [TB*K] expert rank -> expert row
+    int32_t* s_pr = s_er + kFinalizeTokens * a.K;            // [TB*K] primary rank
+    int32_t* s_rs = s_pr + kFinalizeTokens * a.K;            // [TB*R] receive row per (token, rank)
+    const int tid = threadIdx.x;
+    const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kFinalizeTokens;
+    const int nt = static_cast<int>(max(min(static_cast<int64_t>(kFinalizeTokens), a.T - t0), int64_t{0}));
+    const int n = nt * a.K;
+    const int64_t e0 = t0 * a.K;
+
+    for (int i = tid; i < E1; i += kFinalizeThreads) {
         s_eoff[i] = a.expert_offset[i];
         s_poff[i] = a.recv_expert_offset[i];
     }
+    for (int i = tid; i < n; i += kFinalizeThreads) {
+        int e = a.topk_idx[e0 + i];
+        if (e < 0 || e >= a.E) e = -1;
+        s_idx[i] = e;
+        s_er[i] = e >= 0 ? a.ws.erank[e0 + i] : 0;
+        s_pr[i] = e >= 0 ? a.ws.prank[e0 + i] : 0;
+    }
+    for (int i = tid; i < nt * a.R; i += kFinalizeThreads) s_rs[i] = -1;
     __syncthreads();
+
     const int64_t n_entries = static_cast<int64_t>(a.T) * a.K;
     // clamped: after a failed scan the offsets may be stale
     const int64_t n_valid = min(max(static_cast<int64_t>(s_eoff[a.E]), int64_t{0}), n_entries);
     const int64_t n_pairs = min(max(static_cast<int64_t>(s_poff[a.E]), int64_t{0}), a.capacity);
-    const int64_t tid0 = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    const int64_t nthreads = static_cast<int64_t>(gridDim.x) * blockDim.x;
     bool bad = false;
 
+    // entries: expert row; primaries also claim the token's receive row
+    for (int i = tid; i < n; i += kFinalizeThreads) {
+        const int e = s_idx[i];
+        int32_t es = -1;
+        if (e >= 0) {
+            const int tl = i / a.K, k = i - tl * a.K;
+            const int64_t v = static_cast<int64_t>(s_eoff[e]) + s_er[i];
+            if (v >= 0 && v < n_valid) es = static_cast<int32_t>(v); else bad = true;
+            if (is_primary(s_idx + tl * a.K, a.K, k, e, a.m)) {
+                const int64_t rs = static_cast<int64_t>(s_poff[e]) + s_pr[i];
+                if (rs >= 0 && rs < n_pairs) {
+                    s_rs[tl * a.R + e / a.m] = static_cast<int32_t>(rs);
+                    a.recv_src_token[rs] = static_cast<int32_t>(t0 + tl);
+                } else {
+                    bad = true;
+                }
+            }
+        }
+        s_er[i] = es;
+        a.expert_slot[e0 + i] = es;
+    }
+    __syncthreads();
+    for (int i = tid; i < nt * a.R; i += kFinalizeThreads) a.recv_slot[t0 * a.R + i] = s_rs[i];
+    for (int i = tid; i < n; i += kFinalizeThreads) {
+        const int e = s_idx[i];
+        const int32_t es = s_er[i];
+        if (e < 0 || es < 0) continue;
+        const int tl = i / a.K;
+        a.expert_src_row[es] = s_rs[tl * a.R + e / a.m];
+        a.expert_weight[es] = a.topk_w ? a.topk_w[e0 + i] : 0.0f;
+    }
+
+    // tails past the last used rows, spread over all blocks
+    const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kFinalizeThreads + tid;
+    const int64_t gstride = static_cast<int64_t>(gridDim.x) * kFinalizeThreads;
+    for (int64_t i = n_pairs + gtid; i < a.capacity; i += gstride) a.recv_src_token[i] = -1;
+    for (int64_t i = n_valid + gtid; i < n_entries; i += gstride) {
+        a.expert_src_row[i] = -1;
+        a.expert_weight[i] = 0.0f;
+    }
     if (blockIdx.x == 0) {
-        for (int r = threadIdx.x; r <= a.R; r += blockDim.x) {
+        for (int r = tid; r <= a.R; r += kFinalizeThreads) {
             a.rank_offset[r] = s_poff[r * a.m];
             if (r < a.R) a.tokens_per_rank[r] = s_poff[(r + 1) * a.m] - s_poff[r * a.m];
         }
-        if (threadIdx.x == 0) {
-            // move the scan's error bits into the status word, make the next
-            // call's scan start from a fresh ticket and generation
+        if (tid == 0) {
+            // move the scan's error bits into the status word; the next call's
+            // scan starts from a fresh ticket and generation
             const uint32_t k1 = atomicExch(&a.ws.hdr->k1_err, 0u);
             if (k1) atomicOr(a.status, k1);
             a.ws.hdr->ticket = 0u;
             a.ws.hdr->epoch = (a.ws.hdr->epoch + 1u) % kGenMask;
         }
     }
-
-    for (int64_t t = tid0; t < a.T; t += nthreads) {
-        const int32_t* row = a.topk_idx + t * a.K;
-        int32_t* rs_row = a.recv_slot + t * a.R;
-        for (int r = 0; r < a.R; ++r) rs_row[r] = -1;
-        for (int k = 0; k < a.K; ++k) {
-            const int e = row[k];
-            int32_t es = -1;
-            if (e >= 0 && e < a.E) {
-                const int64_t v = static_cast<int64_t>(s_eoff[e]) + a.ws.erank[t * a.K + k];
-                if (v >= 0 && v < n_entries) es = static_cast<int32_t>(v); else bad = true;
-            }
-            a.expert_slot[t * a.K + k] = es;
-        }
-        // receive rows of this token, one per rank that holds one of its experts
-        for (int k = 0; k < a.K; ++k) {
-            const int e = row[k];
-            if (e < 0 || e >= a.E) continue;
-            bool prim = true;
-            for (int k2 = 0; k2 < a.K; ++k2) {
-                const int e2 = row[k2];
-                if (k2 != k && e2 >= 0 && e2 < a.E && e2 / a.m == e / a.m && (e2 < e || (e2 == e && k2 < k))) {
-                    prim = false;
-                    break;
-                }
-            }
-            if (!prim) continue;
-            const int64_t v = static_cast<int64_t>(s_poff[e]) + a.ws.prank[t * a.K + k];
-            if (v >= 0 && v < a.capacity && v < n_pairs) {
-                rs_row[e / a.m] = static_cast<int32_t>(v);
-                a.recv_src_token[v] = static_cast<int32_t>(t);
-            } else {
-                bad = true;
-            }
-        }
-        // expert-major rows point back at the receive row and carry the weight
-        for (int k = 0; k < a.K; ++k) {
-            const int e = row[k];
-            if (e < 0 || e >= a.E) continue;
-            const int32_t es = a.expert_slot[t * a.K + k];
-            if (es < 0) continue;
-            a.expert_src_row[es] = rs_row[e / a.m];
-            a.expert_weight[es] = a.topk_w ? a.topk_w[t * a.K + k] : 0.0f;
-        }
-    }
-    // tails past the last used rows
-    for (int64_t i = n_pairs + tid0; i < a.capacity; i += nthreads) a.recv_src_token[i] = -1;
-    for (int64_t i = n_valid + tid0; i < n_entries; i += nthreads) {
-        a.expert_src_row[i] = -1;
-        a.expert_weight[i] = 0.0f;
-    }
     if (s_poff[a.E] > a.capacity) bad = true;
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
 }
 
 }  // namespace
 
 int32_t default_tile_tokens(int32_t T, int32_t K) {
-    int32_t tt = 1024 / K;                  // about 1024 entries per tile
+    int32_t tt = kMaxTileEntries / K;       // about 2048 entries per scan tile
     if (tt < 1) tt = 1;
     if (T > 0 && tt > T) tt = T;
     return tt;
@@ -410,7 +422,6 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.tile_tokens = L->tile_tokens; sa.num_tiles = L->num_tiles;
     sa.ws = ws; sa.status = L->status;
     sa.tokens_per_expert = L->tokens_per_expert; sa.expert_offset = L->expert_offset;
-    sa.tokens_per_rank = L->tokens_per_rank; sa.rank_offset = L->rank_offset;
     sa.recv_expert_offset = L->recv_expert_offset;
     sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
     const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * 2 * static_cast<size_t>(L->E));
@@ -429,16 +440,15 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     fa.tokens_per_rank = L->tokens_per_rank; fa.rank_offset = L->rank_offset;
     fa.recv_slot = L->recv_slot; fa.expert_slot = L->expert_slot; fa.recv_src_token = L->recv_src_token;
     fa.expert_src_row = L->expert_src_row; fa.expert_weight = L->expert_weight;
-    const int threads = 256;
-    int64_t work = L->T;
-    if (L->capacity > work) work = L->capacity;
-    if (static_cast<int64_t>(L->T) * L->K > work) work = static_cast<int64_t>(L->T) * L->K;
-    int64_t blocks = (work + threads - 1) / threads;
-    const int64_t max_blocks = static_cast<int64_t>(sm_count()) * 8;
-    if (blocks > max_blocks) blocks = max_blocks;
+    int64_t blocks = (static_cast<int64_t>(L->T) + kFinalizeTokens - 1) / kFinalizeTokens;
     if (blocks < 1) blocks = 1;
-    const size_t smem2 = sizeof(int32_t) * 2 * (static_cast<size_t>(L->E) + 1);
-    layout_finalize_kernel<<<static_cast<unsigned>(blocks), threads, smem2, stream>>>(fa);
+    const size_t smem2 = sizeof(int32_t) * (2 * (static_cast<size_t>(L->E) + 1) +
+                                            3 * static_cast<size_t>(kFinalizeTokens) * L->K +
+                                            static_cast<size_t>(kFinalizeTokens) * L->R);
+    err = cudaFuncSetAttribute(layout_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(smem2));
+    if (err != cudaSuccess) return err;
+    layout_finalize_kernel<<<static_cast<unsigned>(blocks), kFinalizeThreads, smem2, stream>>>(fa);
     return cudaGetLastError();
 }
 

@@ -42,10 +42,12 @@ struct LayoutWs {
 enum : uint32_t { kFlagAgg = 1u, kFlagPrefix = 2u, kFlagError = 3u };
 constexpr uint32_t kGenMask = (1u << 30) - 1u;   // generations live in [1, 2^30)
 
-constexpr int kLayoutThreads = 256;
+constexpr int kLayoutThreads = 512;
 constexpr int kLayoutWarps = kLayoutThreads / 32;
 constexpr int kMaxTileEntries = 2048;                                   // T_tile * K
-constexpr int kMaxChunksPerWarp = kMaxTileEntries / (kLayoutWarps * 32);  // 8
+constexpr int kMaxChunksPerWarp = kMaxTileEntries / (kLayoutWarps * 32);  // 4
+constexpr int kFinalizeThreads = 256;
+constexpr int kFinalizeTokens = 32;                                     // tokens per finalize block
 
 __host__ __device__ inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
@@ -190,7 +192,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
                           cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags);
 cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
                             void* recv_x, float* recv_scales, cudaStream_t stream,
-                            int32_t num_channels, int32_t stages, uint64_t timeout_ns);
+                            int32_t num_channels, int32_t stages, int32_t chunk_bytes, uint64_t timeout_ns);
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels);
 LayoutWs layout_workspace(const moe_layout* L);

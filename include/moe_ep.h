@@ -62,11 +62,14 @@ typedef enum moe_status {
 
 /* Optional launch tuning; pass NULL for the defaults. */
 typedef struct moe_tuning {
-    int32_t  num_channels;     /* CTAs ("independent channels") for dispatch / combine; 0 = auto */
-    int32_t  stages;           /* dispatch pipeline depth per channel; 0 = auto                  */
-    uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                  */
-    uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                         */
-    uint32_t reserved;
+    int32_t  num_channels;     /* CTAs ("independent channels") for dispatch / combine; 0 = auto  */
+    int32_t  stages;           /* dispatch pipeline depth per channel, 2..8; 0 = auto             */
+    int32_t  chunk_bytes;      /* dispatch: bf16 bytes of a row per pipeline item (a multiple of
+                                  256, >= 256); 0 = 16384, i.e. whole rows up to hidden 8192     */
+    int32_t  reserved;
+    uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                   */
+    uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                          */
+    uint32_t reserved2;
 } moe_tuning;
 
 /*
