@@ -133,12 +133,13 @@ moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, 
     }
     if (tuning && (tuning->num_channels < 0 || tuning->stages < 0 || tuning->stages > 8 ||
                    (tuning->stages != 0 && tuning->stages < 2) || tuning->chunk_bytes < 0 ||
-                   (tuning->chunk_bytes != 0 && (tuning->chunk_bytes < 256 || tuning->chunk_bytes % 256 != 0))))
+                   (tuning->chunk_bytes != 0 && (tuning->chunk_bytes < 256 || tuning->chunk_bytes % 256 != 0)) ||
+                   tuning->variant < 0 || tuning->variant > 2))
         return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_dispatch(x, hidden, L, fp8 != 0, recv_x, recv_scales,
                                           static_cast<cudaStream_t>(stream), tuning ? tuning->num_channels : 0,
                                           tuning ? tuning->stages : 0, tuning ? tuning->chunk_bytes : 0,
-                                          timeout_of(tuning)));
+                                          tuning ? tuning->variant : 0, timeout_of(tuning)));
 }
 
 moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w, uint16_t* out,

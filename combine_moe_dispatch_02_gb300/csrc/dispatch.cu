@@ -21,6 +21,8 @@
 //     output stage, which TMA bulk stores send to every destination row; the
 //     scales go out with plain stores.
 // x is read from HBM once; the receive rows are written once each.
+#include <climits>
+
 #include "fp8_quant.cuh"
 #include "moe_common.cuh"
 
@@ -217,24 +219,24 @@ dispatch_fp8_kernel(DispatchArgs a) {
         const bool ok = mbar_wait_bounded(&bars[s], static_cast<uint32_t>(k / S) & 1u, a.timeout_ns);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
 
-        // quantise: each half-warp takes one 128-column block per pass
+        // quantise: each group of eight lanes takes one 128-column block per
+        // pass; lane li holds columns li*8.. and 64+li*8.. of the block
         const uint8_t* in = stage_in + static_cast<size_t>(s) * in_bytes;
         uint8_t* out = stage_out + static_cast<size_t>(s) * out_bytes;
-        const int hl = lane & 15;
-        for (int base = warp * 2; base < nb; base += 2 * kWarps) {
-            const int b = base + (lane >> 4);
+        const int li = lane & 7;
+        for (int base = warp * 4; base < nb; base += 4 * kWarps) {
+            const int b = base + (lane >> 3);
             const bool active = b < nb;
-            uint4 raw = make_uint4(0u, 0u, 0u, 0u);
-            if (active) raw = *reinterpret_cast<const uint4*>(in + b * 256 + hl * 16);
-            float amax = absmax8(raw);
-#pragma unroll
-            for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, d));
-            const float sc = __fdiv_rn(amax, 448.0f);
-            const bool fast = scale_is_normal(sc);
-            const float rc = fast ? __frcp_rn(sc) : 0.0f;
+            uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
             if (active) {
-                *reinterpret_cast<uint2*>(out + b * 128 + hl * 8) = quantize8(raw, sc, rc, fast, amax == 0.0f);
-                if (hl == 0) s_scale[s * nbc + b] = sc;
+                va = *reinterpret_cast<const uint4*>(in + b * 256 + li * 16);
+                vb = *reinterpret_cast<const uint4*>(in + b * 256 + 128 + li * 16);
+            }
+            const BlockQuant bq = quantize_block_share(va, vb);
+            if (active) {
+                *reinterpret_cast<uint2*>(out + b * 128 + li * 8) = bq.q0;
+                *reinterpret_cast<uint2*>(out + b * 128 + 64 + li * 8) = bq.q1;
+                if (li == 0) s_scale[s * nbc + b] = bq.scale;
             }
         }
         fence_proxy_async_smem();
@@ -264,11 +266,103 @@ dispatch_fp8_kernel(DispatchArgs a) {
     if (timed_out && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
 }
 
+// 16-byte vector path ------------------------------------------------------
+
+// No shared-memory staging: a warp moves one 512-column segment of one token
+// per item.  Each lane loads two 16-byte vectors, so every load and store
+// instruction of the warp covers whole 32-byte sectors.  bf16: lane l takes
+// columns l*8 and 256 + l*8 of the segment.  FP8: the eight lanes 8g..8g+7
+// hold block g of the segment (lane li: columns li*8 and 64 + li*8 of it) and
+// reduce its amax with shuffles.  Two items are in flight per warp (all their
+// loads are issued before any store).  The destination rows come from
+// recv_slot: lane r holds the slot of rank r and the warp walks the ranks with
+// shuffles.
+constexpr int kLsuThreads = 256;
+constexpr int kSegElems = 512;
+
+__device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+
+template <bool FP8>
+__device__ __forceinline__ int lsu_col(int col0, int lane, int j) {
+    if constexpr (FP8) return col0 + (lane >> 3) * 128 + j * 64 + (lane & 7) * 8;
+    return col0 + j * 256 + lane * 8;
+}
+
+template <bool FP8>
+__global__ void __launch_bounds__(kLsuThreads)
+dispatch_lsu_kernel(DispatchArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kLsuThreads + threadIdx.x) >> 5;
+    const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kLsuThreads) >> 5;
+    const int nseg = (a.H + kSegElems - 1) / kSegElems;
+    const int64_t n_items = static_cast<int64_t>(a.T) * nseg;
+    const int nb_row = a.H / 128;
+    bool bad = false;
+    for (int64_t item0 = warp_id; item0 < n_items; item0 += 2 * n_warps) {
+        uint4 v[2][2];
+        int32_t slot_lane[2];
+        int64_t tok[2];
+        int col0[2];
+        bool live[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t item = item0 + u * n_warps;
+            live[u] = item < n_items;                      // warp-uniform
+            const int64_t t = live[u] ? item / nseg : 0;
+            const int g = live[u] ? static_cast<int>(item - t * nseg) : 0;
+            tok[u] = t;
+            col0[u] = g * kSegElems;
+            slot_lane[u] = (live[u] && lane < a.R) ? __ldg(a.recv_slot + t * a.R + lane) : -1;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int col = lsu_col<FP8>(col0[u], lane, j);
+                v[u][j] = (live[u] && col < a.H) ? ld_nc_v4(a.x + (t * a.H + col) * 2) : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            if (!live[u]) continue;
+            const int64_t t = tok[u];
+            BlockQuant bq;
+            if constexpr (FP8) bq = quantize_block_share(v[u][0], v[u][1]);
+            for (int rbase = 0; rbase < a.R; rbase += 32) {
+                const int32_t my_slot = rbase == 0 ? slot_lane[u]
+                                                   : (lane + rbase < a.R ? __ldg(a.recv_slot + t * a.R + rbase + lane) : -1);
+                const int nr = min(32, a.R - rbase);
+                for (int r = 0; r < nr; ++r) {
+                    const int32_t slot = __shfl_sync(0xffffffffu, my_slot, r);
+                    if (slot < 0) continue;
+                    if (slot >= a.capacity) { bad = true; continue; }
+#pragma unroll
+                    for (int j = 0; j < 2; ++j) {
+                        const int col = lsu_col<FP8>(col0[u], lane, j);
+                        if (col >= a.H) continue;
+                        if constexpr (FP8) {
+                            *reinterpret_cast<uint2*>(a.recv + static_cast<int64_t>(slot) * a.H + col) = j ? bq.q1 : bq.q0;
+                            if (j == 0 && (lane & 7) == 0)
+                                a.recv_scales[static_cast<int64_t>(slot) * nb_row + col / 128] = bq.scale;
+                        } else {
+                            *reinterpret_cast<uint4*>(a.recv + (static_cast<int64_t>(slot) * a.H + col) * 2) = v[u][j];
+                        }
+                    }
+                }
+            }
+        }
+    }
+    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+}
+
 }  // namespace
 
 cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
                             void* recv_x, float* recv_scales, cudaStream_t stream,
-                            int32_t num_channels, int32_t stages, int32_t chunk_bytes, uint64_t timeout_ns) {
+                            int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
+                            uint64_t timeout_ns) {
     if (L->T == 0) return cudaSuccess;
     DispatchArgs a;
     a.x = reinterpret_cast<const uint8_t*>(x);
@@ -287,7 +381,16 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     a.nchunk = (hidden + a.chunk_elems - 1) / a.chunk_elems;   // every chunk non-empty
     a.slot_batch = kSlotBatchInts / L->R;
     if (a.slot_batch < 1) a.slot_batch = 1;
+    // Channels: by default many short ones (about 2 items each for bf16, 4 for
+    // FP8): each CTA issues the loads of all its items at once, and the
+    // scheduler keeps every SM full while earlier channels drain their stores.
+    const int64_t n_items = static_cast<int64_t>(L->T) * a.nchunk;
+    int64_t grid = num_channels > 0 ? num_channels : (n_items + (fp8 ? 3 : 1)) / (fp8 ? 4 : 2);
+    if (grid > n_items) grid = n_items;
+    if (grid < 1) grid = 1;
+    const int64_t items_per_channel = (n_items + grid - 1) / grid;
     int S = stages > 0 ? stages : (fp8 ? 3 : 4);
+    if (S > items_per_channel) S = static_cast<int>(items_per_channel);   // no unused stages
     if (S < 2) S = 2;
     if (S > kMaxStages) S = kMaxStages;
     a.stages = S;
@@ -299,19 +402,30 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     } else {
         smem += static_cast<size_t>(S) * a.chunk_elems * 2;
     }
+    if (variant == 2) {
+        // 16-byte vector path: persistent grid, occupancy-limited
+        const void* fn = fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<true>)
+                             : reinterpret_cast<const void*>(dispatch_lsu_kernel<false>);
+        int per_sm = 0;
+        cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLsuThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) per_sm = 1;
+        const int64_t nseg = (hidden + kSegElems - 1) / kSegElems;
+        const int64_t warps_needed = (static_cast<int64_t>(L->T) * nseg + 1) / 2;
+        int64_t lsu_grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
+        const int64_t need = (warps_needed * 32 + kLsuThreads - 1) / kLsuThreads;
+        if (lsu_grid > need) lsu_grid = need;
+        if (lsu_grid < 1) lsu_grid = 1;
+        if (fp8) dispatch_lsu_kernel<true><<<static_cast<unsigned>(lsu_grid), kLsuThreads, 0, stream>>>(a);
+        else dispatch_lsu_kernel<false><<<static_cast<unsigned>(lsu_grid), kLsuThreads, 0, stream>>>(a);
+        return cudaGetLastError();
+    }
     const void* fn = fp8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel)
                          : reinterpret_cast<const void*>(dispatch_bf16_kernel);
     const int threads = fp8 ? kFp8Threads : 32;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    int per_sm = 0;
-    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, threads, smem);
-    if (err != cudaSuccess) return err;
-    if (per_sm < 1) return cudaErrorInvalidConfiguration;
-    const int64_t n_items = static_cast<int64_t>(L->T) * a.nchunk;
-    int64_t grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
-    if (grid > n_items) grid = n_items;
-    if (grid < 1) grid = 1;
+    if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     if (fp8) dispatch_fp8_kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(a);
     else dispatch_bf16_kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(a);
     return cudaGetLastError();

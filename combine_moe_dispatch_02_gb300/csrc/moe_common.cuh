@@ -192,7 +192,8 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
                           cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags);
 cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
                             void* recv_x, float* recv_scales, cudaStream_t stream,
-                            int32_t num_channels, int32_t stages, int32_t chunk_bytes, uint64_t timeout_ns);
+                            int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
+                            uint64_t timeout_ns);
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels);
 LayoutWs layout_workspace(const moe_layout* L);

@@ -54,7 +54,7 @@ class moe_layout(ctypes.Structure):
 
 class moe_tuning(ctypes.Structure):
     _fields_ = [("num_channels", ctypes.c_int32), ("stages", ctypes.c_int32),
-                ("chunk_bytes", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("chunk_bytes", ctypes.c_int32), ("variant", ctypes.c_int32),
                 ("wait_timeout_ns", ctypes.c_uint64), ("debug_flags", ctypes.c_uint32),
                 ("reserved2", ctypes.c_uint32)]
 
@@ -115,10 +115,10 @@ def _stream(stream: torch.cuda.Stream | None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
-def _tuning(num_channels=0, stages=0, chunk_bytes=0, wait_timeout_ns=0, debug_flags=0):
-    if not (num_channels or stages or chunk_bytes or wait_timeout_ns or debug_flags):
+def _tuning(num_channels=0, stages=0, chunk_bytes=0, variant=0, wait_timeout_ns=0, debug_flags=0):
+    if not (num_channels or stages or chunk_bytes or variant or wait_timeout_ns or debug_flags):
         return None
-    return ctypes.pointer(moe_tuning(num_channels, stages, chunk_bytes, 0, wait_timeout_ns, debug_flags, 0))
+    return ctypes.pointer(moe_tuning(num_channels, stages, chunk_bytes, variant, wait_timeout_ns, debug_flags, 0))
 
 
 def moe_layout_bytes(T: int, K: int, E: int, R: int, capacity: int) -> int:

@@ -1,52 +1,73 @@
-// Test-only kernel: compares the dispatch kernel's quotient
-// (moe::scaled_quotient with r = __frcp_rn(s)) against CUDA's IEEE division
-// __fdiv_rn(x, s) for every bf16 value x with |x| <= amax, over a list of
-// block maxima amax (s = __fdiv_rn(amax, 448)).  Counts bitwise mismatches
-// and records the first few.  Every index is bounded by the array sizes.
+// Test-only kernel: checks the dispatch kernels' fast FP8 arithmetic against
+// CUDA's IEEE operations, for a list of bf16 block maxima amax:
+//   scale:      moe::block_scale(amax)  vs __fdiv_rn(amax, 448)  (every amax)
+//   reciprocal: moe::block_recip(s)     vs __frcp_rn(s)          (fast range)
+//   quotient:   moe::div_by_scale(x, s, r) vs __fdiv_rn(x, s) for every bf16
+//               x with |x| <= amax, bit for bit where |x| >= 2^-100 and
+//               |x/s| >= 2^-100 (the claimed exact range),
+//   codes:      their E4M3 codes, everywhere.
+// The first few quotient and code mismatches are recorded.  Every index is
+// bounded by the array sizes.
 #include <cstdint>
 
 #include "fp8_quant.cuh"
 
 namespace {
 
-__global__ void div_check_kernel(const uint16_t* amax_bits, int n_amax, unsigned long long* mismatches,
-                                 uint32_t* examples, int max_examples, unsigned long long* checked) {
+__device__ void record(unsigned long long* counter, uint32_t* examples, int max_examples, uint32_t a,
+                       uint32_t b, uint32_t c, uint32_t d) {
+    const unsigned long long slot = atomicAdd(counter, 1ull);
+    if (slot < static_cast<unsigned long long>(max_examples)) {
+        examples[4 * slot + 0] = a;
+        examples[4 * slot + 1] = b;
+        examples[4 * slot + 2] = c;
+        examples[4 * slot + 3] = d;
+    }
+}
+
+__global__ void div_check_kernel(const uint16_t* amax_bits, int n_amax, unsigned long long* counters,
+                                 uint32_t* examples, int max_examples) {
     const int a_idx = blockIdx.y;
     if (a_idx >= n_amax) return;
     const float amax = __uint_as_float(static_cast<uint32_t>(amax_bits[a_idx]) << 16);
     const float s = __fdiv_rn(amax, 448.0f);
-    if (!moe::scale_is_normal(s)) return;
-    const float r = __frcp_rn(s);
-    unsigned long long local_bad = 0, local_n = 0;
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        if (__float_as_uint(moe::block_scale(amax)) != __float_as_uint(s)) atomicAdd(&counters[3], 1ull);
+        if (moe::amax_in_fast_range(amax) && __float_as_uint(moe::block_recip(s)) != __float_as_uint(__frcp_rn(s)))
+            atomicAdd(&counters[4], 1ull);
+    }
+    if (!moe::amax_in_fast_range(amax)) return;
+    const float r = moe::block_recip(s);
+    unsigned local_n = 0;
     for (uint32_t xb = blockIdx.x * blockDim.x + threadIdx.x; xb < 65536u; xb += gridDim.x * blockDim.x) {
         const float x = __uint_as_float(xb << 16);
         if (!(fabsf(x) <= amax)) continue;            // skips NaN and values beyond the block max
         ++local_n;
-        const float q_fast = moe::scaled_quotient(x, s, r, true);
+        const float q_fast = moe::div_by_scale(x, s, r);
         const float q_ieee = __fdiv_rn(x, s);
-        if (__float_as_uint(q_fast) != __float_as_uint(q_ieee)) {
-            ++local_bad;
-            const unsigned long long slot = atomicAdd(mismatches, 1ull);
-            if (slot < static_cast<unsigned long long>(max_examples)) {
-                examples[4 * slot + 0] = amax_bits[a_idx];
-                examples[4 * slot + 1] = xb;
-                examples[4 * slot + 2] = __float_as_uint(q_fast);
-                examples[4 * slot + 3] = __float_as_uint(q_ieee);
-            }
-        }
+        const bool in_range = x == 0.0f || (fabsf(x) >= 0x1p-100f && fabsf(q_ieee) >= 0x1p-100f);
+        if (in_range && __float_as_uint(q_fast) != __float_as_uint(q_ieee))
+            record(&counters[0], examples, max_examples, amax_bits[a_idx], xb, __float_as_uint(q_fast),
+                   __float_as_uint(q_ieee));
+        const uint32_t c_fast = moe::e4m3x2(q_fast, 0.0f) & 0xffu;
+        const uint32_t c_ieee = moe::e4m3x2(q_ieee, 0.0f) & 0xffu;
+        if (c_fast != c_ieee)
+            record(&counters[1], examples + 4 * max_examples, max_examples, amax_bits[a_idx], xb, c_fast, c_ieee);
     }
-    (void)local_bad;
-    const unsigned warp_n = __reduce_add_sync(0xffffffffu, static_cast<unsigned>(local_n));
-    if ((threadIdx.x & 31) == 0) atomicAdd(checked, static_cast<unsigned long long>(warp_n));
+    const unsigned warp_n = __reduce_add_sync(0xffffffffu, local_n);
+    if ((threadIdx.x & 31) == 0) atomicAdd(&counters[2], static_cast<unsigned long long>(warp_n));
 }
 
 }  // namespace
 
-extern "C" int fp8_div_check(const uint16_t* amax_bits, int n_amax, unsigned long long* mismatches,
-                             uint32_t* examples, int max_examples, unsigned long long* checked) {
+// counters: [quotient mismatches, code mismatches, pairs checked, scale mismatches,
+//            reciprocal mismatches];
+// examples: 2 * max_examples records of 4 words.
+extern "C" int fp8_div_check(const uint16_t* amax_bits, int n_amax, unsigned long long* counters,
+                             uint32_t* examples, int max_examples) {
     if (n_amax <= 0 || n_amax > 65535) return 1;
     dim3 grid(64, static_cast<unsigned>(n_amax));
-    div_check_kernel<<<grid, 256>>>(amax_bits, n_amax, mismatches, examples, max_examples, checked);
+    div_check_kernel<<<grid, 256>>>(amax_bits, n_amax, counters, examples, max_examples);
     if (cudaGetLastError() != cudaSuccess) return 2;
     return cudaDeviceSynchronize() == cudaSuccess ? 0 : 3;
 }

@@ -1,8 +1,11 @@
-"""The FP8 dispatch divides each value by its block scale with Markstein's
-FMA-corrected quotient (see csrc/fp8_quant.cuh).  This checks it against
-CUDA's IEEE division __fdiv_rn bit for bit: every bf16 value x with
-|x| <= amax, for a few thousand block maxima amax spread over the whole
-bf16 exponent range (s = amax / 448)."""
+"""The FP8 dispatch replaces divisions by fused multiply-adds (Markstein's
+correction step, csrc/fp8_quant.cuh).  This checks it against CUDA's IEEE
+operations: the block scale amax/448 and the reciprocal 1/s for every
+positive finite bf16 block maximum, and the quotient x/s for every bf16
+value x with |x| <= amax, for a few thousand block maxima spread over the
+whole bf16 exponent range: scales and reciprocals agree bit for bit, the
+quotients wherever the method is claimed exact, and the E4M3 codes
+everywhere."""
 import ctypes
 import os
 import subprocess
@@ -29,9 +32,22 @@ def divcheck():
                            "-o", so])
     lib = ctypes.CDLL(so)
     lib.fp8_div_check.restype = ctypes.c_int
-    lib.fp8_div_check.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int,
-                                  ctypes.c_void_p]
+    lib.fp8_div_check.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     return lib
+
+
+def _run(divcheck, pats):
+    amax = torch.tensor(sorted(pats), dtype=torch.int32).to(torch.int16).cuda()
+    counters = torch.zeros(5, dtype=torch.int64, device="cuda")
+    ex = torch.zeros(2 * 16 * 4, dtype=torch.int32, device="cuda")
+    rc = divcheck.fp8_div_check(amax.data_ptr(), amax.numel(), counters.data_ptr(), ex.data_ptr(), 16)
+    assert rc == 0
+    return [int(v) for v in counters.cpu()], ex.view(2, 16, 4).cpu().numpy()
+
+
+def test_scale_and_reciprocal_for_every_bf16_block_max(divcheck):
+    (_, _, _, scale_bad, recip_bad), _ = _run(divcheck, range(0x0001, 0x7F80))
+    assert scale_bad == 0 and recip_bad == 0
 
 
 def test_fast_quotient_matches_ieee_division(divcheck):
@@ -42,13 +58,8 @@ def test_fast_quotient_matches_ieee_division(divcheck):
     pats |= {e << 7 for e in range(1, 255)}
     pats |= {(e << 7) | 0x7F for e in range(0, 255)}
     pats |= {0x0001, 0x0080, 0x7F7F, 0x3F80, 0x4000, 0x43E0}
-    amax = torch.tensor(sorted(pats), dtype=torch.int32).to(torch.int16).cuda()
-    mism = torch.zeros(1, dtype=torch.int64, device="cuda")
-    checked = torch.zeros(1, dtype=torch.int64, device="cuda")
-    ex = torch.zeros(64, dtype=torch.int32, device="cuda")
-    rc = divcheck.fp8_div_check(amax.data_ptr(), amax.numel(), mism.data_ptr(), ex.data_ptr(), 16,
-                                checked.data_ptr())
-    assert rc == 0
-    n_bad, n = int(mism.item()), int(checked.item())
-    assert n > 50_000_000
-    assert n_bad == 0, ex.view(-1, 4)[:min(n_bad, 16)].cpu().numpy()
+    (q_bad, code_bad, n, scale_bad, recip_bad), ex = _run(divcheck, pats)
+    assert n > 20_000_000                       # pairs inside the fast scale range
+    assert q_bad == 0, ex[0][:min(q_bad, 16)]
+    assert code_bad == 0, ex[1][:min(code_bad, 16)]
+    assert scale_bad == 0 and recip_bad == 0

@@ -26,12 +26,14 @@ def _gpu():
 def test_workload_parity_full_size(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl)
-    g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8)
-    assert g["status"] == 0 and o["status"] == 0
-    assert_parity(g, o, fp8=wl.fp8)
-    # combine is bit-exact in practice (same fma chain)
-    assert np.array_equal(g["out"], o["out"])
+    assert o["status"] == 0
+    for variant in (0, 1, 2):
+        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8, variant=variant)
+        assert g["status"] == 0
+        assert_parity(g, o, fp8=wl.fp8)
+        # combine is bit-exact in practice (same fma chain)
+        assert np.array_equal(g["out"], o["out"])
 
 
 @pytest.mark.parametrize("T,H,E,R,K,mask,dups,fp8,seed", [
@@ -48,13 +50,14 @@ def test_workload_parity_full_size(name):
     (2500, 128, 256, 32, 8, 0.0, False, False, 10),  # many tiles, wide ranks
     (4096, 64, 1024, 256, 32, 0.0, False, False, 11),  # the documented maxima of E, R and K
 ])
-def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed):
+@pytest.mark.parametrize("variant", [1, 2])
+def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed, variant):
     idx = random_routing(T, K, E, seed, mask_frac=mask, allow_duplicates=dups)
     w = random_weights(T, K, seed)
     g_ = torch.Generator().manual_seed(seed + 1)
     x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
     y = torch.randn(T * K, H, generator=g_).to(torch.bfloat16)
-    g = gpu_run(x, idx, w, y, E, R, fp8=fp8)
+    g = gpu_run(x, idx, w, y, E, R, fp8=fp8, variant=variant)
     o = oracle_run(x, idx, w, y, E, R, fp8=fp8)
     assert g["status"] == 0 and o["status"] == 0
     assert_parity(g, o, fp8=fp8)
@@ -98,9 +101,10 @@ def test_fp8_special_blocks():
     x[4] *= 1e-30
     x[5, 256:384] = torch.tensor([1e-38] * 127 + [1.0])
     x = x.to(torch.bfloat16)
-    g = gpu_run(x, idx, None, None, E, R, fp8=True)
     o = oracle_run(x, idx, None, None, E, R, fp8=True)
-    assert_parity(g, o, fp8=True)
+    for variant in (1, 2):
+        g = gpu_run(x, idx, None, None, E, R, fp8=True, variant=variant)
+        assert_parity(g, o, fp8=True)
 
 
 def test_repeated_calls_reuse_workspace():
@@ -143,12 +147,15 @@ def test_tuning_variants_agree():
     wl = WORKLOADS["dsv3"].scaled(512)
     inp = make_inputs(wl)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R)
-    for ch, st in [(1, 2), (4, 3), (16, 8), (1000, 0)]:
-        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, num_channels=ch, stages=st)
+    for ch, st, cb, var in [(1, 2, 0, 1), (4, 3, 2048, 1), (16, 8, 4096, 1), (1000, 0, 0, 1),
+                            (1, 0, 0, 2), (5, 0, 0, 2), (3000, 0, 0, 2)]:
+        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, num_channels=ch, stages=st,
+                    chunk_bytes=cb, variant=var)
         assert_parity(g, o)
     o8 = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True)
-    for ch, st in [(1, 2), (7, 4)]:
-        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True, num_channels=ch, stages=st)
+    for ch, st, cb, var in [(1, 2, 0, 1), (7, 4, 2048, 1), (3, 0, 0, 2), (999, 0, 0, 2)]:
+        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True, num_channels=ch, stages=st,
+                    chunk_bytes=cb, variant=var)
         assert_parity(g, o8, fp8=True)
 
 
