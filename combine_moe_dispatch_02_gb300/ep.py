@@ -34,8 +34,10 @@ MOE_DEVERR_TIMEOUT = 0x4
 
 MOE_DEBUG_STALL_FIRST_TILE = 0x1
 
-EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_dispatch_layout", "moe_dispatch", "moe_combine",
-            "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
+EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
+            "moe_dispatch", "moe_combine", "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
+
+MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 class moe_layout(ctypes.Structure):
@@ -82,6 +84,9 @@ def lib() -> ctypes.CDLL:
         L.moe_layout_init.argtypes = [ctypes.POINTER(moe_layout), i32, i32, i32, i32, i64, P, ctypes.c_size_t]
         L.moe_dispatch_layout.restype = ctypes.c_int
         L.moe_dispatch_layout.argtypes = [P, P, i32, i32, ctypes.POINTER(moe_layout), P, ctypes.POINTER(moe_tuning)]
+        L.moe_dispatch_layout_noalloc.restype = ctypes.c_int
+        L.moe_dispatch_layout_noalloc.argtypes = [P, P, i32, i32, ctypes.POINTER(moe_layout), P,
+                                                  ctypes.POINTER(moe_tuning)]
         L.moe_dispatch.restype = ctypes.c_int
         L.moe_dispatch.argtypes = [P, i32, ctypes.POINTER(moe_layout), ctypes.c_int, P, P, P,
                                    ctypes.POINTER(moe_tuning)]
@@ -182,6 +187,17 @@ def moe_dispatch_layout(topk_idx: torch.Tensor, topk_w: torch.Tensor | None, num
     assert topk_w is None or (topk_w.dtype == torch.float32 and topk_w.is_contiguous())
     _check(lib().moe_dispatch_layout(_ptr(topk_idx), _ptr(topk_w), num_experts, num_ranks, ctypes.byref(L.c),
                                      _stream(stream), _tuning(**tuning)), "moe_dispatch_layout")
+
+
+def moe_dispatch_layout_noalloc(topk_idx: torch.Tensor, topk_w: torch.Tensor | None, num_experts: int,
+                                num_ranks: int, L: moe_layout, stream=None, **tuning) -> None:
+    """The allocation-free layout entry point.  `L` is a plain moe_layout whose
+    sizes, output pointers and status pointer the caller has filled in; its
+    workspace fields are not used."""
+    assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous()
+    assert topk_w is None or (topk_w.dtype == torch.float32 and topk_w.is_contiguous())
+    _check(lib().moe_dispatch_layout_noalloc(_ptr(topk_idx), _ptr(topk_w), num_experts, num_ranks, ctypes.byref(L),
+                                             _stream(stream), _tuning(**tuning)), "moe_dispatch_layout_noalloc")
 
 
 def moe_dispatch(x: torch.Tensor, L: Layout, fp8: bool, recv_x: torch.Tensor,

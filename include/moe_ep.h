@@ -138,6 +138,42 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w,
                                int32_t num_experts, int32_t num_ranks,
                                moe_layout* L, void* stream, const moe_tuning* tuning);
 
+/* Dispatch layout for callers that cannot allocate device memory.
+ *
+ * Some callers of this library never call cudaMalloc themselves: a plugin
+ * inside a host framework that hands out every device buffer from its own
+ * allocator and refuses side allocations, or a serving loop that has fixed
+ * its device memory at start-up and must not pay an allocation's latency and
+ * implicit device synchronisation on the request path.  Such a caller can
+ * still own the layout's outputs (they are what it keeps), but not the scan's
+ * scratch space.  This entry point has no counterpart on the pages: it is the
+ * same operation as moe_dispatch_layout, with identical results, and it
+ * allocates nothing.
+ *
+ * The scan workspace is a device array of MOE_NOALLOC_SCRATCH_BYTES compiled
+ * into the library; every GPU that loads the library holds it until the
+ * process exits.  Sizes whose workspace does not fit (moe_layout_bytes minus
+ * the outputs; about 8 * T * K bytes plus 16 * E bytes per 2048-entry tile)
+ * return MOE_ERR_UNSUPPORTED.
+ *
+ * Fields of *L that are read: T, K, E, R, capacity (>= T * min(K, R)), the
+ * ten output pointers and status, all caller-owned device memory of the sizes
+ * listed above; tile_tokens, num_tiles, workspace and workspace_bytes are
+ * ignored and left unchanged.  No moe_layout_init call is needed.
+ *
+ * All calls share the one array, which keeps the previous call's contents;
+ * each call clears the parts that must start at zero.  Calls that overlap on
+ * the GPU (on different streams without ordering, or from several threads)
+ * race on it.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it: make that
+ * first call before any stream capture.  No cudaMalloc, cudaFree or other
+ * allocating routine is called. */
+#define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, const float* topk_w,
+                                       int32_t num_experts, int32_t num_ranks,
+                                       moe_layout* L, void* stream, const moe_tuning* tuning);
+
 /* Dispatch: for every pair with recv_slot[t,r] >= 0 write token t's row into
  * receive row recv_slot[t,r]: each token once per destination rank, rows in
  * expert-contiguous order.
