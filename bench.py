@@ -4,8 +4,9 @@
 One step = dispatch layout (2 kernels) -> bf16 dispatch -> combine over the
 DeepSeek-V3-shaped workload: 4096 tokens, hidden 7168, 256 experts over 8
 virtual ranks, top-8 (seeded synthetic routing and activations).  Inputs are
-resident in HBM; L2 is flushed (a 256 MB write) between timed steps, outside
-the CUDA-event brackets.  Prints one JSON line.
+resident in HBM; L2 is flushed (a 256 MB write, then a 256 MB read of another
+buffer) between timed steps, outside the CUDA-event brackets.  Prints one
+JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -125,6 +126,26 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ------------------------------------------------------------------ L2 flush
+
+class L2Flush:
+    """Between timed steps: write a 256 MB buffer (twice the 129 MB L2), then
+    read a second one, so that the step starts with an L2 holding only clean
+    lines of unrelated data -- no cached inputs, and no dirty flush lines whose
+    write-back would be charged to the next kernel."""
+
+    def __init__(self, dev):
+        import torch
+        self.a = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.b = torch.ones(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+        self.n = 0
+
+    def __call__(self):
+        self.n += 1
+        self.a.fill_(self.n)
+        self.b.max()
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -148,7 +169,7 @@ def run_ours(args, rank, world, local_rank):
     recv, _ = ep.alloc_recv(L, H, False, device=dev)
     recv8, scales8 = ep.alloc_recv(L, H, True, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
 
     def step(evs=None):
@@ -165,7 +186,7 @@ def run_ours(args, rank, world, local_rank):
             evs[3].record(stream)
 
     for _ in range(args.warmup):
-        flush.fill_(1)
+        flush()
         step()
     torch.cuda.synchronize(dev)
     st, flags = ep.moe_layout_read_status(L, stream)
@@ -185,7 +206,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
-        flush.fill_(s)            # L2 flush, outside the event brackets
+        flush()                   # L2 flush, outside the event brackets
         step(events[s])
     torch.cuda.synchronize(dev)
     if world > 1:
@@ -209,7 +230,7 @@ def run_ours(args, rank, world, local_rank):
     # FP8 dispatch, timed the same way (secondary figure)
     ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 3))]
     for e in ev8:
-        flush.fill_(3)
+        flush()
         e[0].record(stream)
         ep.moe_dispatch(x, L, True, recv8, scales8, stream)
         e[1].record(stream)
@@ -237,7 +258,7 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) activations, softmax top-8 routing of N(0,1) logits)",
         "config": {"workload": "DeepSeek-V3 shape: 4096 tokens, hidden 7168, 256 experts / 8 virtual ranks, top-8",
                    "T": T, "H": H, "E": E, "R": R, "K": K, "n_pairs": n_pairs, "capacity": L.capacity,
-                   "step": "layout + bf16 dispatch + combine", "l2": "flushed (256 MB write) between steps",
+                   "step": "layout + bf16 dispatch + combine", "l2": "flushed between steps (256 MB write, then 256 MB read of another buffer)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "ops": {

@@ -147,9 +147,10 @@ moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, c
     if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
     if (L->T > 0 && (!y || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y) || !aligned16(out) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) != 0) return MOE_ERR_INVALID_ARG;
-    if (tuning && tuning->num_channels < 0) return MOE_ERR_INVALID_ARG;
+    if (tuning && (tuning->num_channels < 0 || tuning->variant < 0 || tuning->variant > 2)) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_combine(y, hidden, L, topk_w, out, static_cast<cudaStream_t>(stream),
-                                         tuning ? tuning->num_channels : 0));
+                                         tuning ? tuning->num_channels : 0, tuning ? tuning->variant : 0,
+                                         timeout_of(tuning)));
 }
 
 moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* flags_out) {

@@ -58,6 +58,7 @@ __device__ __forceinline__ uint4 pack8(const float (&acc)[8]) {
 template <int KT>
 __global__ void __launch_bounds__(kCombineThreads)
 combine_kernel(CombineArgs a) {
+    pdl_wait();
     const int64_t n_items = static_cast<int64_t>(a.T) * a.H8;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * kCombineThreads;
     bool bad = false;
@@ -108,6 +109,7 @@ combine_kernel(CombineArgs a) {
         }
         st_stream_v4(a.out + it, pack8(acc));
     }
+    pdl_trigger();
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
 }
 
@@ -122,14 +124,130 @@ cudaError_t launch_k(const CombineArgs& a, cudaStream_t stream, int32_t num_chan
     const int64_t need = (n_items + kCombineThreads - 1) / kCombineThreads;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    combine_kernel<KT><<<static_cast<unsigned>(grid), kCombineThreads, 0, stream>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(combine_kernel<KT>, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), 0, stream, a);
+}
+
+// TMA-staged variant --------------------------------------------------------
+//
+// Items are (token, 1024-column chunk).  A producer warp reads the token's K
+// slots and weights once, then for each item waits for a free stage, posts
+// the expected byte count on the stage's "full" mbarrier and issues one TMA
+// bulk copy per valid entry (lane k copies row expert_slot[t,k]'s chunk).
+// Four consumer warps (one 16-byte column group per thread) wait on "full",
+// run the fp32 fma chain over k = 0..K-1 reading the rows from shared memory,
+// store 16 bytes of output and release the stage through its "empty"
+// mbarrier.  Every wait is bounded.
+constexpr int kTmaCE = 1024;                        // columns per item
+constexpr int kTmaConsumers = kTmaCE / 8;           // one 16-byte group per consumer thread
+constexpr int kTmaThreads = 32 + kTmaConsumers;     // producer warp + 4 consumer warps
+constexpr int kTmaMaxK = 8;
+constexpr int kTmaStages = 4;
+
+struct TmaStageMeta {
+    float w[kTmaMaxK];
+    uint32_t ok;                                    // bit k: entry k has a valid row
+};
+
+__global__ void __launch_bounds__(kTmaThreads)
+combine_tma_kernel(CombineArgs a, uint64_t timeout_ns) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_wait();
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* empty = full + kTmaStages;
+    TmaStageMeta* meta = reinterpret_cast<TmaStageMeta*>(smem + 16 * kTmaStages);
+    uint8_t* stage0 = smem + align_up(16 * kTmaStages + sizeof(TmaStageMeta) * kTmaStages, 128);
+    const size_t stage_bytes = static_cast<size_t>(a.K) * kTmaCE * 2;
+    const int H = a.H8 * 8;
+    const int nchunk = (H + kTmaCE - 1) / kTmaCE;
+    const int64_t n_items = static_cast<int64_t>(a.T) * nchunk;
+    const int64_t i0 = n_items * blockIdx.x / gridDim.x;
+    const int n = static_cast<int>(n_items * (blockIdx.x + 1) / gridDim.x - i0);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (n <= 0) return;
+    if (tid == 0) {
+        for (int s = 0; s < kTmaStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kTmaConsumers / 32);
+        }
+        fence_mbar_init();
+    }
+    __syncthreads();
+    bool bad = false, timed_out = false;
+
+    if (warp == 0) {
+        // ---------------- producer
+        int64_t cur_t = -1;
+        int32_t slot = -1;
+        float wk = 0.0f;
+        uint32_t ok = 0;
+        for (int i = 0; i < n; ++i) {
+            const int s = i % kTmaStages;
+            const int64_t item = i0 + i;
+            const int64_t t = item / nchunk;
+            const int c = static_cast<int>(item - t * nchunk);
+            if (t != cur_t) {
+                cur_t = t;
+                slot = lane < a.K ? __ldg(a.expert_slot + t * a.K + lane) : -1;
+                wk = lane < a.K ? __ldg(a.w + t * a.K + lane) : 0.0f;
+                bad |= slot >= a.n_rows;
+                ok = __ballot_sync(0xffffffffu, slot >= 0 && slot < a.n_rows);
+            }
+            if (i >= kTmaStages) {
+                const bool got = mbar_wait_bounded(&empty[s], static_cast<uint32_t>(i / kTmaStages - 1) & 1u, timeout_ns);
+                if (__any_sync(0xffffffffu, !got)) { timed_out = true; break; }
+            }
+            const int elems = min(kTmaCE, H - c * kTmaCE);
+            const uint32_t bytes = static_cast<uint32_t>(elems) * 2u;
+            if (lane < a.K) meta[s].w[lane] = wk;
+            if (lane == 0) meta[s].ok = ok;
+            __syncwarp();
+            if (lane == 0) mbar_arrive_expect_tx(&full[s], bytes * __popc(ok));
+            __syncwarp();
+            if ((ok >> lane) & 1u)
+                bulk_g2s(stage0 + s * stage_bytes + static_cast<size_t>(lane) * kTmaCE * 2,
+                         reinterpret_cast<const uint8_t*>(a.y) + (static_cast<int64_t>(slot) * H + c * kTmaCE) * 2,
+                         bytes, &full[s]);
+        }
+    } else {
+        // ---------------- consumers
+        const int j = tid - 32;                     // 16-byte column group within the chunk
+        for (int i = 0; i < n; ++i) {
+            const int s = i % kTmaStages;
+            const int64_t item = i0 + i;
+            const int64_t t = item / nchunk;
+            const int c = static_cast<int>(item - t * nchunk);
+            const bool got = mbar_wait_bounded(&full[s], static_cast<uint32_t>(i / kTmaStages) & 1u, timeout_ns);
+            if (__any_sync(0xffffffffu, !got)) { timed_out = true; break; }
+            const int elems = min(kTmaCE, H - c * kTmaCE);
+            const uint32_t ok = meta[s].ok;
+            if (j * 8 < elems) {
+                float acc[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+                const uint8_t* st = stage0 + s * stage_bytes + j * 16;
+                for (int k = 0; k < a.K; ++k) {
+                    if (!((ok >> k) & 1u)) continue;
+                    const uint4 v = *reinterpret_cast<const uint4*>(st + static_cast<size_t>(k) * kTmaCE * 2);
+                    fma8(acc, meta[s].w[k], v);
+                }
+                st_stream_v4(a.out + t * a.H8 + c * (kTmaCE / 8) + j, pack8(acc));
+            }
+            __syncwarp();
+            if (lane == 0) {
+                asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(smem_addr(&empty[s])) : "memory");
+            }
+        }
+    }
+    pdl_trigger();
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+    if (__syncthreads_or(timed_out) && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
-                           uint16_t* out, cudaStream_t stream, int32_t num_channels) {
+                           uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
+                           uint64_t timeout_ns) {
     if (L->T == 0) return cudaSuccess;
     CombineArgs a;
     a.y = reinterpret_cast<const uint4*>(y);
@@ -139,6 +257,23 @@ cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* 
     a.T = L->T; a.K = L->K; a.H8 = hidden / 8;
     a.n_rows = static_cast<int64_t>(L->T) * L->K;
     a.status = L->status;
+    if (variant == 1 && L->K <= kTmaMaxK) {
+        const size_t smem = align_up(16 * kTmaStages + sizeof(TmaStageMeta) * kTmaStages, 128) +
+                            static_cast<size_t>(kTmaStages) * L->K * kTmaCE * 2;
+        cudaError_t err = cudaFuncSetAttribute(combine_tma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+        int per_sm = 0;
+        err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_tma_kernel, kTmaThreads, smem);
+        if (err != cudaSuccess) return err;
+        if (per_sm < 1) per_sm = 1;
+        const int64_t n_items = static_cast<int64_t>(L->T) * ((hidden + kTmaCE - 1) / kTmaCE);
+        int64_t grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
+        if (grid > n_items) grid = n_items;
+        if (grid < 1) grid = 1;
+        return launch_pdl(combine_tma_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTmaThreads), smem, stream, a,
+                          timeout_ns);
+    }
     switch (L->K) {
         case 1: return launch_k<1>(a, stream, num_channels);
         case 2: return launch_k<2>(a, stream, num_channels);

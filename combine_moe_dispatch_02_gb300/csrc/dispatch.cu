@@ -73,6 +73,7 @@ __device__ __forceinline__ void smem_carve(uint8_t* smem, const DispatchArgs& a,
 __global__ void __launch_bounds__(32)
 dispatch_bf16_kernel(DispatchArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_wait();
     const ItemRange rg = channel_items(a);
     if (rg.n <= 0) return;
     uint64_t* bars;
@@ -142,6 +143,7 @@ dispatch_bf16_kernel(DispatchArgs a) {
             if (lane == 0) issue_load(k - 1 + S);
         }
     }
+    pdl_trigger();          // many waves: let the next kernel launch only as channels finish
     bulk_wait_all();
     const uint32_t any_bad = __ballot_sync(0xffffffffu, bad);
     const uint32_t any_tmo = __ballot_sync(0xffffffffu, timed_out);
@@ -159,6 +161,7 @@ dispatch_bf16_kernel(DispatchArgs a) {
 __global__ void __launch_bounds__(kFp8Threads)
 dispatch_fp8_kernel(DispatchArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_wait();
     const ItemRange rg = channel_items(a);
     if (rg.n <= 0) return;
     uint64_t* bars;
@@ -261,6 +264,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
             a.recv_scales[static_cast<int64_t>(slot) * nb_row + c * nbc + b] = s_scale[s * nbc + b];
         }
     }
+    pdl_trigger();
     if (warp == 0) bulk_wait_all();
     if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
     if (timed_out && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
@@ -296,6 +300,7 @@ __device__ __forceinline__ int lsu_col(int col0, int lane, int j) {
 template <bool FP8>
 __global__ void __launch_bounds__(kLsuThreads)
 dispatch_lsu_kernel(DispatchArgs a) {
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = (static_cast<int64_t>(blockIdx.x) * kLsuThreads + threadIdx.x) >> 5;
     const int64_t n_warps = (static_cast<int64_t>(gridDim.x) * kLsuThreads) >> 5;
@@ -354,6 +359,7 @@ dispatch_lsu_kernel(DispatchArgs a) {
             }
         }
     }
+    pdl_trigger();
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
 }
 
@@ -416,9 +422,11 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
         const int64_t need = (warps_needed * 32 + kLsuThreads - 1) / kLsuThreads;
         if (lsu_grid > need) lsu_grid = need;
         if (lsu_grid < 1) lsu_grid = 1;
-        if (fp8) dispatch_lsu_kernel<true><<<static_cast<unsigned>(lsu_grid), kLsuThreads, 0, stream>>>(a);
-        else dispatch_lsu_kernel<false><<<static_cast<unsigned>(lsu_grid), kLsuThreads, 0, stream>>>(a);
-        return cudaGetLastError();
+        if (fp8)
+            return launch_pdl(dispatch_lsu_kernel<true>, dim3(static_cast<unsigned>(lsu_grid)), dim3(kLsuThreads), 0,
+                              stream, a);
+        return launch_pdl(dispatch_lsu_kernel<false>, dim3(static_cast<unsigned>(lsu_grid)), dim3(kLsuThreads), 0,
+                          stream, a);
     }
     const void* fn = fp8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel)
                          : reinterpret_cast<const void*>(dispatch_bf16_kernel);
@@ -426,9 +434,8 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-    if (fp8) dispatch_fp8_kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(a);
-    else dispatch_bf16_kernel<<<static_cast<unsigned>(grid), threads, smem, stream>>>(a);
-    return cudaGetLastError();
+    if (fp8) return launch_pdl(dispatch_fp8_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, a);
+    return launch_pdl(dispatch_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, a);
 }
 
 }  // namespace moe

@@ -42,17 +42,26 @@ struct ScanArgs {
     uint32_t debug_flags;
 };
 
-// True if entry k of a token (expert e, rank e/m) is the primary entry of its
-// rank: no other valid entry of the token on the same rank has a smaller id,
-// and no earlier entry has the same id.
-__device__ __forceinline__ bool is_primary(const int32_t* row, int K, int k, int e, int m) {
-    const int r = e / m;
-    for (int k2 = 0; k2 < K; ++k2) {
-        if (k2 == k) continue;
-        const int e2 = row[k2];
-        if (e2 >= 0 && e2 / m == r && (e2 < e || (e2 == e && k2 < k))) return false;
+// Primary flags of one token's K entries: entry k (expert e, rank r) is
+// primary if no other valid entry of the token on rank r has a smaller id and
+// no earlier entry has the same id.  `rank_of` maps experts to ranks (a table,
+// so the K^2 comparisons need no divisions).
+__device__ __forceinline__ void mark_primaries(const int32_t* row, uint8_t* prim, int K, const int32_t* rank_of) {
+    for (int k = 0; k < K; ++k) {
+        const int e = row[k];
+        bool p = e >= 0;
+        if (p) {
+            const int r = rank_of[e];
+            for (int k2 = 0; k2 < K; ++k2) {
+                const int e2 = row[k2];
+                if (k2 != k && e2 >= 0 && rank_of[e2] == r && (e2 < e || (e2 == e && k2 < k))) {
+                    p = false;
+                    break;
+                }
+            }
+        }
+        prim[k] = p ? 1 : 0;
     }
-    return true;
 }
 
 constexpr uint32_t kWaitTimedOut = 4u;
@@ -83,16 +92,21 @@ layout_scan_kernel(ScanArgs a) {
     int32_t* s_hist = s_idx + kMaxTileEntries;            // [warps][2E]
     int32_t* s_prefix = s_hist + kLayoutWarps * twoE;     // [2E]
     int32_t* s_agg = s_prefix + twoE;                     // [2E]
+    int32_t* s_rank = s_agg + twoE;                       // [E]: rank of expert e
+    uint8_t* s_prim = reinterpret_cast<uint8_t*>(s_rank + a.E);   // [kMaxTileEntries]: primary entry?
     __shared__ int s_tile;
     __shared__ uint32_t s_gen;
     __shared__ int s_lb_count, s_lb_final;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();          // one wave of CTAs: the finalize grid may become resident now
     if (tid == 0) {
         s_tile = static_cast<int>(atomicAdd(&a.ws.hdr->ticket, 1u));
         s_gen = (ld_relaxed_gpu(&a.ws.hdr->epoch) & kGenMask) + 1u;
     }
     for (int i = tid; i < kLayoutWarps * twoE; i += kLayoutThreads) s_hist[i] = 0;
+    for (int e = tid; e < a.E; e += kLayoutThreads) s_rank[e] = e / a.m;
     __syncthreads();
     const int tile = s_tile;
     const uint32_t gen = s_gen;
@@ -112,6 +126,10 @@ layout_scan_kernel(ScanArgs a) {
     }
     if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_EXPERT_ID);
 
+    // 1b. primary flags, one thread per token
+    for (int tl = tid; tl < nt; tl += kLayoutThreads) mark_primaries(s_idx + tl * a.K, s_prim + tl * a.K, a.K, s_rank);
+    __syncthreads();
+
     // 2. order-preserving ranks inside the tile: warp w owns a contiguous
     //    segment of 32-entry chunks and keeps its own histogram
     const int seg = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
@@ -123,11 +141,7 @@ layout_scan_kernel(ScanArgs a) {
         if (c * 32 >= seg) continue;            // warp-uniform
         const int i = warp * seg + c * 32 + lane;
         const int e = (i < n) ? s_idx[i] : -1;
-        bool prim = false;
-        if (e >= 0) {
-            const int tl = i / a.K, k = i - tl * a.K;
-            prim = is_primary(s_idx + tl * a.K, a.K, k, e, a.m);
-        }
+        const bool prim = e >= 0 && s_prim[i] != 0;
         const uint32_t peers = __match_any_sync(0xffffffffu, e);
         const uint32_t pmask = __ballot_sync(0xffffffffu, prim) & peers;
         const uint32_t lt = lanemask_lt();
@@ -240,7 +254,7 @@ layout_scan_kernel(ScanArgs a) {
         const int e = ent_e[c];
         const int64_t gi = static_cast<int64_t>(t0) * a.K + warp * seg + c * 32 + lane;
         a.ws.erank[gi] = s_prefix[e] + my_hist[e] + lr_e[c];
-        if (lr_p[c] >= 0) a.ws.prank[gi] = s_prefix[a.E + e] + my_hist[a.E + e] + lr_p[c];
+        a.ws.prank[gi] = lr_p[c] >= 0 ? s_prefix[a.E + e] + my_hist[a.E + e] + lr_p[c] : -1;
     }
 
     // 6. the last tile holds the totals: counts and offsets (warp w < 2 scans half w)
@@ -292,15 +306,19 @@ layout_finalize_kernel(FinalArgs a) {
     int32_t* s_er = s_idx + kFinalizeTokens * a.K;           // [TB*K] expert rank -> expert row
     int32_t* s_pr = s_er + kFinalizeTokens * a.K;            // [TB*K] primary rank
     int32_t* s_rs = s_pr + kFinalizeTokens * a.K;            // [TB*R] receive row per (token, rank)
+    int32_t* s_rank = s_rs + kFinalizeTokens * a.R;          // [E] rank of expert e
     const int tid = threadIdx.x;
     const int64_t t0 = static_cast<int64_t>(blockIdx.x) * kFinalizeTokens;
     const int nt = static_cast<int>(max(min(static_cast<int64_t>(kFinalizeTokens), a.T - t0), int64_t{0}));
     const int n = nt * a.K;
     const int64_t e0 = t0 * a.K;
 
+    pdl_wait();
+    pdl_trigger();          // one wave of CTAs: the dispatch grid may become resident now
     for (int i = tid; i < E1; i += kFinalizeThreads) {
         s_eoff[i] = a.expert_offset[i];
         s_poff[i] = a.recv_expert_offset[i];
+        if (i < a.E) s_rank[i] = i / a.m;
     }
     for (int i = tid; i < n; i += kFinalizeThreads) {
         int e = a.topk_idx[e0 + i];
@@ -318,18 +336,22 @@ layout_finalize_kernel(FinalArgs a) {
     const int64_t n_pairs = min(max(static_cast<int64_t>(s_poff[a.E]), int64_t{0}), a.capacity);
     bool bad = false;
 
-    // entries: expert row; primaries also claim the token's receive row
+    // i / K without an integer division: (i + 0.5) / K is at least 1/(2K) away
+    // from an integer and i < 2^10 here, so the fp32 product's error (below
+    // 2^-13) cannot change its integer part
+    const float inv_k = 1.0f / static_cast<float>(a.K);
+    // entries: expert row; primaries (prank >= 0) also claim the token's receive row
     for (int i = tid; i < n; i += kFinalizeThreads) {
         const int e = s_idx[i];
         int32_t es = -1;
         if (e >= 0) {
-            const int tl = i / a.K, k = i - tl * a.K;
+            const int tl = __float2int_rz((static_cast<float>(i) + 0.5f) * inv_k);
             const int64_t v = static_cast<int64_t>(s_eoff[e]) + s_er[i];
             if (v >= 0 && v < n_valid) es = static_cast<int32_t>(v); else bad = true;
-            if (is_primary(s_idx + tl * a.K, a.K, k, e, a.m)) {
+            if (s_pr[i] >= 0) {
                 const int64_t rs = static_cast<int64_t>(s_poff[e]) + s_pr[i];
                 if (rs >= 0 && rs < n_pairs) {
-                    s_rs[tl * a.R + e / a.m] = static_cast<int32_t>(rs);
+                    s_rs[tl * a.R + s_rank[e]] = static_cast<int32_t>(rs);
                     a.recv_src_token[rs] = static_cast<int32_t>(t0 + tl);
                 } else {
                     bad = true;
@@ -345,8 +367,8 @@ layout_finalize_kernel(FinalArgs a) {
         const int e = s_idx[i];
         const int32_t es = s_er[i];
         if (e < 0 || es < 0) continue;
-        const int tl = i / a.K;
-        a.expert_src_row[es] = s_rs[tl * a.R + e / a.m];
+        const int tl = __float2int_rz((static_cast<float>(i) + 0.5f) * inv_k);
+        a.expert_src_row[es] = s_rs[tl * a.R + s_rank[e]];
         a.expert_weight[es] = a.topk_w ? a.topk_w[e0 + i] : 0.0f;
     }
 
@@ -424,12 +446,12 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.tokens_per_expert = L->tokens_per_expert; sa.expert_offset = L->expert_offset;
     sa.recv_expert_offset = L->recv_expert_offset;
     sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
-    const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * 2 * static_cast<size_t>(L->E));
+    const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * 2 * static_cast<size_t>(L->E) +
+                                            static_cast<size_t>(L->E)) + kMaxTileEntries;
     cudaError_t err = cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem1));
     if (err != cudaSuccess) return err;
-    layout_scan_kernel<<<L->num_tiles, kLayoutThreads, smem1, stream>>>(sa);
-    err = cudaGetLastError();
+    err = launch_pdl(layout_scan_kernel, dim3(L->num_tiles), dim3(kLayoutThreads), smem1, stream, sa);
     if (err != cudaSuccess) return err;
 
     FinalArgs fa;
@@ -444,12 +466,12 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     if (blocks < 1) blocks = 1;
     const size_t smem2 = sizeof(int32_t) * (2 * (static_cast<size_t>(L->E) + 1) +
                                             3 * static_cast<size_t>(kFinalizeTokens) * L->K +
-                                            static_cast<size_t>(kFinalizeTokens) * L->R);
+                                            static_cast<size_t>(kFinalizeTokens) * L->R + L->E);
     err = cudaFuncSetAttribute(layout_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem2));
     if (err != cudaSuccess) return err;
-    layout_finalize_kernel<<<static_cast<unsigned>(blocks), kFinalizeThreads, smem2, stream>>>(fa);
-    return cudaGetLastError();
+    return launch_pdl(layout_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFinalizeThreads), smem2,
+                      stream, fa);
 }
 
 }  // namespace moe

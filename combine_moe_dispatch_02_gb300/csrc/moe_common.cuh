@@ -5,6 +5,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include <cuda_runtime.h>
 
@@ -184,6 +185,34 @@ __device__ __forceinline__ void st_stream_v4(uint4* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// Programmatic dependent launch ---------------------------------------------
+//
+// Every kernel of the path is launched with programmatic stream serialization
+// (launch_pdl below), so its CTAs may be scheduled while the previous kernel in
+// the stream is still finishing.  Each kernel therefore calls pdl_wait() before
+// its first global memory access: it returns once the previous grid has
+// completed and its writes are visible (and at once when there is none).
+// pdl_trigger() lets the next kernel's launch begin early; it never affects
+// correctness, only when the dependent CTAs become resident.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 }  // namespace moe
 
 // Launch helpers implemented in the per-operator translation units.
@@ -195,7 +224,8 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
                             uint64_t timeout_ns);
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
-                           uint16_t* out, cudaStream_t stream, int32_t num_channels);
+                           uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
+                           uint64_t timeout_ns);
 LayoutWs layout_workspace(const moe_layout* L);
 size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles);
 int32_t default_tile_tokens(int32_t T, int32_t K);
