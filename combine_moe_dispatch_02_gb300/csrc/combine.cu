@@ -124,7 +124,10 @@ cudaError_t launch_k(const CombineArgs& a, cudaStream_t stream, int32_t num_chan
     const int64_t need = (n_items + kCombineThreads - 1) / kCombineThreads;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
-    return launch_pdl(combine_kernel<KT>, dim3(static_cast<unsigned>(grid)), dim3(kCombineThreads), 0, stream, a);
+    // An ordinary launch: letting the combine grid become resident while the
+    // many-wave dispatch drains (programmatic launch) measured ~15% slower.
+    combine_kernel<KT><<<static_cast<unsigned>(grid), kCombineThreads, 0, stream>>>(a);
+    return cudaGetLastError();
 }
 
 // TMA-staged variant --------------------------------------------------------
@@ -271,8 +274,8 @@ cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* 
         int64_t grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
         if (grid > n_items) grid = n_items;
         if (grid < 1) grid = 1;
-        return launch_pdl(combine_tma_kernel, dim3(static_cast<unsigned>(grid)), dim3(kTmaThreads), smem, stream, a,
-                          timeout_ns);
+        combine_tma_kernel<<<static_cast<unsigned>(grid), kTmaThreads, smem, stream>>>(a, timeout_ns);
+        return cudaGetLastError();
     }
     switch (L->K) {
         case 1: return launch_k<1>(a, stream, num_channels);

@@ -42,26 +42,39 @@ struct ScanArgs {
     uint32_t debug_flags;
 };
 
-// Primary flags of one token's K entries: entry k (expert e, rank r) is
-// primary if no other valid entry of the token on rank r has a smaller id and
-// no earlier entry has the same id.  `rank_of` maps experts to ranks (a table,
-// so the K^2 comparisons need no divisions).
-__device__ __forceinline__ void mark_primaries(const int32_t* row, uint8_t* prim, int K, const int32_t* rank_of) {
-    for (int k = 0; k < K; ++k) {
-        const int e = row[k];
-        bool p = e >= 0;
-        if (p) {
-            const int r = rank_of[e];
-            for (int k2 = 0; k2 < K; ++k2) {
-                const int e2 = row[k2];
-                if (k2 != k && e2 >= 0 && rank_of[e2] == r && (e2 < e || (e2 == e && k2 < k))) {
-                    p = false;
-                    break;
-                }
-            }
+// Width of a tile's count vector: E expert counts, E primary counts, padded to
+// a multiple of 4 so that the look-back can move it in 16-byte pieces.
+__host__ __device__ __forceinline__ int vec_width(int E) { return (2 * E + 3) / 4 * 4; }
+
+// Key of a valid entry: (rank << 16) | expert (experts < 2^16); -1 if masked.
+// Two keys share a rank iff their upper halves are equal, and then compare like
+// their expert ids.
+//
+// Entry k of a token is primary if no other valid entry of the token on the
+// same rank has a smaller id and no earlier entry has the same id.
+// The token's keys are read eight at a time (independent loads in flight)
+// and compared without early exits.
+__device__ __forceinline__ bool is_primary_key(const int32_t* row_keys, int K, int k, int32_t key) {
+    bool prim = true;
+    for (int k0 = 0; k0 < K; k0 += 8) {
+        int32_t kk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) kk[u] = (k0 + u < K) ? row_keys[k0 + u] : -1;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int k2 = k0 + u;
+            const int32_t key2 = kk[u];
+            prim &= !(k2 != k && key2 >= 0 && (key2 >> 16) == (key >> 16) && (key2 < key || (key2 == key && k2 < k)));
         }
-        prim[k] = p ? 1 : 0;
     }
+    return prim;
+}
+
+// i / K for i < 2^11 and K <= 32 without an integer division: (i + 0.5) / K is
+// at least 1/(2K) >= 2^-6 away from an integer, and the fp32 product's error is
+// below 2^11 * 2^-23 = 2^-12, so truncation gives the exact quotient.
+__device__ __forceinline__ int div_small(int i, float inv_k) {
+    return __float2int_rz((static_cast<float>(i) + 0.5f) * inv_k);
 }
 
 constexpr uint32_t kWaitTimedOut = 4u;
@@ -86,14 +99,15 @@ __device__ uint32_t wait_tile_flag(const uint32_t* flag, uint32_t gen, const uin
 
 __global__ void __launch_bounds__(kLayoutThreads, 1)
 layout_scan_kernel(ScanArgs a) {
-    extern __shared__ int32_t smem[];
-    const int twoE = 2 * a.E;
-    int32_t* s_idx = smem;                                // [kMaxTileEntries]
-    int32_t* s_hist = s_idx + kMaxTileEntries;            // [warps][2E]
-    int32_t* s_prefix = s_hist + kLayoutWarps * twoE;     // [2E]
-    int32_t* s_agg = s_prefix + twoE;                     // [2E]
-    int32_t* s_rank = s_agg + twoE;                       // [E]: rank of expert e
-    uint8_t* s_prim = reinterpret_cast<uint8_t*>(s_rank + a.E);   // [kMaxTileEntries]: primary entry?
+    extern __shared__ __align__(16) int32_t smem[];
+    const int W = vec_width(a.E);
+    const int nvec = W / 4;
+    int32_t* s_key = smem;                                            // [kMaxTileEntries]
+    int32_t* s_hist = s_key + kMaxTileEntries;                        // [warps][W]
+    int32_t* s_prefix = s_hist + kLayoutWarps * W;                    // [W]
+    int32_t* s_agg = s_prefix + W;                                    // [W]
+    int4* s_part = reinterpret_cast<int4*>(s_agg + W);                // [kLayoutThreads]
+    int32_t* s_rank = reinterpret_cast<int32_t*>(s_part + kLayoutThreads);   // [E]
     __shared__ int s_tile;
     __shared__ uint32_t s_gen;
     __shared__ int s_lb_count, s_lb_final;
@@ -105,7 +119,7 @@ layout_scan_kernel(ScanArgs a) {
         s_tile = static_cast<int>(atomicAdd(&a.ws.hdr->ticket, 1u));
         s_gen = (ld_relaxed_gpu(&a.ws.hdr->epoch) & kGenMask) + 1u;
     }
-    for (int i = tid; i < kLayoutWarps * twoE; i += kLayoutThreads) s_hist[i] = 0;
+    for (int i = tid; i < kLayoutWarps * W; i += kLayoutThreads) s_hist[i] = 0;
     for (int e = tid; e < a.E; e += kLayoutThreads) s_rank[e] = e / a.m;
     __syncthreads();
     const int tile = s_tile;
@@ -117,32 +131,44 @@ layout_scan_kernel(ScanArgs a) {
     const int nt = min(a.tile_tokens, a.T - t0);
     const int n = nt * a.K;
 
-    // 1. the tile's entries; ids outside [-1, E) are flagged and masked
+    // 1. the tile's entries as keys; ids outside [-1, E) are flagged and masked
     bool bad = false;
     for (int i = tid; i < n; i += kLayoutThreads) {
-        int e = a.topk_idx[static_cast<int64_t>(t0) * a.K + i];
-        if (e < -1 || e >= a.E) { bad = true; e = -1; }
-        s_idx[i] = e;
+        const int e = a.topk_idx[static_cast<int64_t>(t0) * a.K + i];
+        int32_t key = -1;
+        if (e >= 0 && e < a.E) key = (s_rank[e] << 16) | e;
+        else if (e != -1) bad = true;
+        s_key[i] = key;
     }
     if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_EXPERT_ID);
 
-    // 1b. primary flags, one thread per token
-    for (int tl = tid; tl < nt; tl += kLayoutThreads) mark_primaries(s_idx + tl * a.K, s_prim + tl * a.K, a.K, s_rank);
-    __syncthreads();
-
     // 2. order-preserving ranks inside the tile: warp w owns a contiguous
-    //    segment of 32-entry chunks and keeps its own histogram
+    //    segment of 32-entry chunks and keeps its own histogram.  Lanes with the
+    //    same expert are found with one ballot per bit of the expert id.
     const int seg = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
+    const int nbits = 32 - __clz(max(a.E - 1, 1));
+    const float inv_k = 1.0f / static_cast<float>(a.K);
     int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
-    int32_t* my_hist = s_hist + warp * twoE;
+    int32_t* my_hist = s_hist + warp * W;
 #pragma unroll
     for (int c = 0; c < kMaxChunksPerWarp; ++c) {
         lr_e[c] = -1; lr_p[c] = -1; ent_e[c] = -1;
         if (c * 32 >= seg) continue;            // warp-uniform
         const int i = warp * seg + c * 32 + lane;
-        const int e = (i < n) ? s_idx[i] : -1;
-        const bool prim = e >= 0 && s_prim[i] != 0;
-        const uint32_t peers = __match_any_sync(0xffffffffu, e);
+        const int32_t key = (i < n) ? s_key[i] : -1;
+        const int e = key >= 0 ? (key & 0xffff) : -1;
+        bool prim = false;
+        if (key >= 0) {
+            const int tl = div_small(i, inv_k);
+            prim = is_primary_key(s_key + tl * a.K, a.K, i - tl * a.K, key);
+        }
+        uint32_t peers = __ballot_sync(0xffffffffu, key >= 0);
+        if (key < 0) peers = ~peers;
+        for (int b = 0; b < nbits; ++b) {
+            const bool bit = (e >> b) & 1;
+            const uint32_t bb = __ballot_sync(0xffffffffu, bit);
+            peers &= bit ? bb : ~bb;
+        }
         const uint32_t pmask = __ballot_sync(0xffffffffu, prim) & peers;
         const uint32_t lt = lanemask_lt();
         int base_e = 0, base_p = 0;
@@ -162,12 +188,12 @@ layout_scan_kernel(ScanArgs a) {
     __syncthreads();
 
     // 3. exclusive scan of the per-warp histograms; tile aggregate
-    for (int col = tid; col < twoE; col += kLayoutThreads) {
+    for (int col = tid; col < W; col += kLayoutThreads) {
         int run = 0;
 #pragma unroll
         for (int w = 0; w < kLayoutWarps; ++w) {
-            const int v = s_hist[w * twoE + col];
-            s_hist[w * twoE + col] = run;
+            const int v = s_hist[w * W + col];
+            s_hist[w * W + col] = run;
             run += v;
         }
         s_agg[col] = run;
@@ -179,17 +205,21 @@ layout_scan_kernel(ScanArgs a) {
     const bool stall = (a.debug_flags & MOE_DEBUG_STALL_FIRST_TILE) && tile == 0;
     bool failed = false;
     if (tile == 0) {
-        for (int col = tid; col < twoE; col += kLayoutThreads) a.ws.tile_incl[col] = s_agg[col];
+        for (int col = tid; col < W; col += kLayoutThreads) a.ws.tile_incl[col] = s_agg[col];
         __threadfence();
         __syncthreads();
         if (tid == 0 && !stall) st_release_gpu(&a.ws.tile_flag[0], (gen << 2) | kFlagPrefix);
     } else {
-        int32_t* my_agg = a.ws.tile_agg + static_cast<int64_t>(tile) * twoE;
-        for (int col = tid; col < twoE; col += kLayoutThreads) my_agg[col] = s_agg[col];
+        int32_t* my_agg = a.ws.tile_agg + static_cast<int64_t>(tile) * W;
+        for (int col = tid; col < W; col += kLayoutThreads) my_agg[col] = s_agg[col];
         __threadfence();
         __syncthreads();
         if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagAgg);
 
+        // the window's vectors are summed by `groups` thread groups, each taking
+        // every groups-th predecessor, with 16-byte loads: one round of loads
+        const int groups = max(1, min(8, kLayoutThreads / nvec));
+        const int g = tid / nvec, v = tid - (tid / nvec) * nvec;
         int hi = tile - 1;                      // nearest tile not yet summed
         while (true) {
             if (warp == 0) {
@@ -218,17 +248,28 @@ layout_scan_kernel(ScanArgs a) {
             __syncthreads();
             const int cnt = s_lb_count, fin = s_lb_final;
             if (cnt < 0) { failed = true; break; }
-            // sum the window's vectors: independent L2 loads, unrolled so that
-            // several are in flight per thread
-            for (int col = tid; col < twoE; col += kLayoutThreads) {
-                int acc = 0;
+            if (g < groups) {
+                int4 acc = make_int4(0, 0, 0, 0);
 #pragma unroll 8
-                for (int q = 0; q < cnt; ++q) {
+                for (int q = g; q < cnt; q += groups) {
                     const int64_t j = hi - q;
                     const int32_t* src = (fin && q == cnt - 1) ? a.ws.tile_incl : a.ws.tile_agg;
-                    acc += __ldcg(src + j * twoE + col);
+                    const int4 x = __ldcg(reinterpret_cast<const int4*>(src + j * W) + v);
+                    acc.x += x.x; acc.y += x.y; acc.z += x.z; acc.w += x.w;
                 }
-                s_prefix[col] += acc;
+                s_part[g * nvec + v] = acc;
+            }
+            __syncthreads();
+            for (int c4 = tid; c4 < nvec; c4 += kLayoutThreads) {
+                int4 sum = s_part[c4];
+                for (int gg = 1; gg < groups; ++gg) {
+                    const int4 x = s_part[gg * nvec + c4];
+                    sum.x += x.x; sum.y += x.y; sum.z += x.z; sum.w += x.w;
+                }
+                int4* p = reinterpret_cast<int4*>(s_prefix) + c4;
+                int4 cur = *p;
+                cur.x += sum.x; cur.y += sum.y; cur.z += sum.z; cur.w += sum.w;
+                *p = cur;
             }
             hi -= cnt;
             __syncthreads();
@@ -238,8 +279,8 @@ layout_scan_kernel(ScanArgs a) {
         if (failed) {
             if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagError);
         } else {
-            int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * twoE;
-            for (int col = tid; col < twoE; col += kLayoutThreads) my_incl[col] = s_prefix[col] + s_agg[col];
+            int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * W;
+            for (int col = tid; col < W; col += kLayoutThreads) my_incl[col] = s_prefix[col] + s_agg[col];
             __threadfence();
             __syncthreads();
             if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagPrefix);
@@ -247,7 +288,7 @@ layout_scan_kernel(ScanArgs a) {
     }
     if (failed) return;
 
-    // 5. per-entry ranks including the tile prefix
+    // 5. per-entry ranks including the tile prefix (prank = -1: not primary)
 #pragma unroll
     for (int c = 0; c < kMaxChunksPerWarp; ++c) {
         if (ent_e[c] < 0) continue;
@@ -264,16 +305,16 @@ layout_scan_kernel(ScanArgs a) {
         int carry = 0;
         for (int base = 0; base < a.E; base += 32) {
             const int e = base + lane;
-            const int v = (e < a.E) ? s_prefix[half * a.E + e] + s_agg[half * a.E + e] : 0;
-            int incl = v;
+            const int v2 = (e < a.E) ? s_prefix[half * a.E + e] + s_agg[half * a.E + e] : 0;
+            int incl = v2;
 #pragma unroll
             for (int d = 1; d < 32; d <<= 1) {
                 const int u = __shfl_up_sync(0xffffffffu, incl, d);
                 if (lane >= d) incl += u;
             }
             if (e < a.E) {
-                off[e] = carry + incl - v;
-                if (!half) a.tokens_per_expert[e] = v;
+                off[e] = carry + incl - v2;
+                if (!half) a.tokens_per_expert[e] = v2;
             }
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
@@ -336,16 +377,13 @@ layout_finalize_kernel(FinalArgs a) {
     const int64_t n_pairs = min(max(static_cast<int64_t>(s_poff[a.E]), int64_t{0}), a.capacity);
     bool bad = false;
 
-    // i / K without an integer division: (i + 0.5) / K is at least 1/(2K) away
-    // from an integer and i < 2^10 here, so the fp32 product's error (below
-    // 2^-13) cannot change its integer part
-    const float inv_k = 1.0f / static_cast<float>(a.K);
+    const float inv_k = 1.0f / static_cast<float>(a.K);     // i < 2^10 here: div_small is exact
     // entries: expert row; primaries (prank >= 0) also claim the token's receive row
     for (int i = tid; i < n; i += kFinalizeThreads) {
         const int e = s_idx[i];
         int32_t es = -1;
         if (e >= 0) {
-            const int tl = __float2int_rz((static_cast<float>(i) + 0.5f) * inv_k);
+            const int tl = div_small(i, inv_k);
             const int64_t v = static_cast<int64_t>(s_eoff[e]) + s_er[i];
             if (v >= 0 && v < n_valid) es = static_cast<int32_t>(v); else bad = true;
             if (s_pr[i] >= 0) {
@@ -367,7 +405,7 @@ layout_finalize_kernel(FinalArgs a) {
         const int e = s_idx[i];
         const int32_t es = s_er[i];
         if (e < 0 || es < 0) continue;
-        const int tl = __float2int_rz((static_cast<float>(i) + 0.5f) * inv_k);
+        const int tl = div_small(i, inv_k);
         a.expert_src_row[es] = s_rs[tl * a.R + s_rank[e]];
         a.expert_weight[es] = a.topk_w ? a.topk_w[e0 + i] : 0.0f;
     }
@@ -410,8 +448,8 @@ int32_t default_tile_tokens(int32_t T, int32_t K) {
 size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles) {
     size_t b = sizeof(WsHeader);
     b = align_up(b + sizeof(uint32_t) * num_tiles, 256);
-    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * 2 * E, 256);
-    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * 2 * E, 256);
+    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * vec_width(E), 256);
+    b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * vec_width(E), 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
     return b;
@@ -426,9 +464,9 @@ LayoutWs layout_workspace(const moe_layout* L) {
     ws.tile_flag = reinterpret_cast<uint32_t*>(p + off);
     off = align_up(off + sizeof(uint32_t) * L->num_tiles, 256);
     ws.tile_agg = reinterpret_cast<int32_t*>(p + off);
-    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * 2 * L->E, 256);
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * vec_width(L->E), 256);
     ws.tile_incl = reinterpret_cast<int32_t*>(p + off);
-    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * 2 * L->E, 256);
+    off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * vec_width(L->E), 256);
     ws.erank = reinterpret_cast<int32_t*>(p + off);
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->T) * L->K, 256);
     ws.prank = reinterpret_cast<int32_t*>(p + off);
@@ -446,8 +484,8 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.tokens_per_expert = L->tokens_per_expert; sa.expert_offset = L->expert_offset;
     sa.recv_expert_offset = L->recv_expert_offset;
     sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
-    const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * 2 * static_cast<size_t>(L->E) +
-                                            static_cast<size_t>(L->E)) + kMaxTileEntries;
+    const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
+                                            static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
     cudaError_t err = cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem1));
     if (err != cudaSuccess) return err;

@@ -187,11 +187,12 @@ __device__ __forceinline__ void st_stream_v4(uint4* p, uint4 v) {
 
 // Programmatic dependent launch ---------------------------------------------
 //
-// Every kernel of the path is launched with programmatic stream serialization
-// (launch_pdl below), so its CTAs may be scheduled while the previous kernel in
-// the stream is still finishing.  Each kernel therefore calls pdl_wait() before
-// its first global memory access: it returns once the previous grid has
-// completed and its writes are visible (and at once when there is none).
+// The layout and dispatch kernels are launched with programmatic stream
+// serialization (launch_pdl below), so their CTAs may be scheduled while the
+// previous kernel in the stream is still finishing.  Every kernel of the path
+// calls pdl_wait() before its first global memory access: it returns once the
+// previous grid has completed and its writes are visible (at once when the
+// kernel was launched normally or nothing precedes it).
 // pdl_trigger() lets the next kernel's launch begin early; it never affects
 // correctness, only when the dependent CTAs become resident.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
