@@ -18,9 +18,10 @@
 //     a decoupled look-back over the 2E-wide count vectors of earlier tiles
 //     (one warp inspects 32 predecessors at a time; the vectors are summed
 //     with many loads in flight per thread) gives the tile's prefix.  Every
-//     wait is bounded.  The last tile also writes the count / offset outputs.
-//  2. layout_finalize_kernel: one block per 32 tokens stages the tokens'
-//     entries and ranks in shared memory, adds the expert offsets and writes
+//     wait is bounded.
+//  2. layout_finalize_kernel: one block per 32 tokens derives the expert
+//     offsets from the last tile's totals (a block-wide scan), stages the
+//     tokens' entries and ranks in shared memory, adds the offsets and writes
 //     recv_slot, expert_slot, recv_src_token, expert_src_row and
 //     expert_weight with coalesced row writes, plus the tails past the last
 //     used row.
@@ -36,8 +37,6 @@ struct ScanArgs {
     int32_t tile_tokens, num_tiles;
     LayoutWs ws;
     uint32_t* status;
-    // count / offset outputs, written by the last tile
-    int32_t *tokens_per_expert, *expert_offset, *recv_expert_offset;
     uint64_t timeout_ns;
     uint32_t debug_flags;
 };
@@ -150,39 +149,50 @@ layout_scan_kernel(ScanArgs a) {
     const float inv_k = 1.0f / static_cast<float>(a.K);
     int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
     int32_t* my_hist = s_hist + warp * W;
+    // 2a. keys, primary flags and peer masks of all chunks (independent work)
+    int32_t key[kMaxChunksPerWarp];
+    bool prim[kMaxChunksPerWarp];
+    uint32_t peers[kMaxChunksPerWarp];
+#pragma unroll
+    for (int c = 0; c < kMaxChunksPerWarp; ++c) {
+        const int i = warp * seg + c * 32 + lane;
+        key[c] = (c * 32 < seg && i < n) ? s_key[i] : -1;
+        prim[c] = false;
+        if (key[c] >= 0) {
+            const int tl = div_small(i, inv_k);
+            prim[c] = is_primary_key(s_key + tl * a.K, a.K, i - tl * a.K, key[c]);
+        }
+        peers[c] = __ballot_sync(0xffffffffu, key[c] >= 0);
+        if (key[c] < 0) peers[c] = ~peers[c];
+    }
+    for (int b = 0; b < nbits; ++b) {
+#pragma unroll
+        for (int c = 0; c < kMaxChunksPerWarp; ++c) {
+            const bool bit = (key[c] >> b) & 1;
+            const uint32_t bb = __ballot_sync(0xffffffffu, bit);
+            peers[c] &= bit ? bb : ~bb;
+        }
+    }
+    // 2b. per-warp histogram updates, chunk by chunk
+    const uint32_t lt = lanemask_lt();
 #pragma unroll
     for (int c = 0; c < kMaxChunksPerWarp; ++c) {
         lr_e[c] = -1; lr_p[c] = -1; ent_e[c] = -1;
         if (c * 32 >= seg) continue;            // warp-uniform
-        const int i = warp * seg + c * 32 + lane;
-        const int32_t key = (i < n) ? s_key[i] : -1;
-        const int e = key >= 0 ? (key & 0xffff) : -1;
-        bool prim = false;
-        if (key >= 0) {
-            const int tl = div_small(i, inv_k);
-            prim = is_primary_key(s_key + tl * a.K, a.K, i - tl * a.K, key);
-        }
-        uint32_t peers = __ballot_sync(0xffffffffu, key >= 0);
-        if (key < 0) peers = ~peers;
-        for (int b = 0; b < nbits; ++b) {
-            const bool bit = (e >> b) & 1;
-            const uint32_t bb = __ballot_sync(0xffffffffu, bit);
-            peers &= bit ? bb : ~bb;
-        }
-        const uint32_t pmask = __ballot_sync(0xffffffffu, prim) & peers;
-        const uint32_t lt = lanemask_lt();
+        const int e = key[c] >= 0 ? (key[c] & 0xffff) : -1;
+        const uint32_t pmask = __ballot_sync(0xffffffffu, prim[c]) & peers[c];
         int base_e = 0, base_p = 0;
         if (e >= 0) { base_e = my_hist[e]; base_p = my_hist[a.E + e]; }
         __syncwarp();
-        if (e >= 0 && (peers & lt) == 0) {       // lowest lane of its group updates
-            my_hist[e] = base_e + __popc(peers);
+        if (e >= 0 && (peers[c] & lt) == 0) {    // lowest lane of its group updates
+            my_hist[e] = base_e + __popc(peers[c]);
             my_hist[a.E + e] = base_p + __popc(pmask);
         }
         __syncwarp();
         if (e >= 0) {
             ent_e[c] = e;
-            lr_e[c] = base_e + __popc(peers & lt);
-            if (prim) lr_p[c] = base_p + __popc(pmask & lt);
+            lr_e[c] = base_e + __popc(peers[c] & lt);
+            if (prim[c]) lr_p[c] = base_p + __popc(pmask & lt);
         }
     }
     __syncthreads();
@@ -297,41 +307,60 @@ layout_scan_kernel(ScanArgs a) {
         a.ws.erank[gi] = s_prefix[e] + my_hist[e] + lr_e[c];
         a.ws.prank[gi] = lr_p[c] >= 0 ? s_prefix[a.E + e] + my_hist[a.E + e] + lr_p[c] : -1;
     }
-
-    // 6. the last tile holds the totals: counts and offsets (warp w < 2 scans half w)
-    if (tile == a.num_tiles - 1 && warp < 2) {
-        const int half = warp;
-        int32_t* off = half ? a.recv_expert_offset : a.expert_offset;
-        int carry = 0;
-        for (int base = 0; base < a.E; base += 32) {
-            const int e = base + lane;
-            const int v2 = (e < a.E) ? s_prefix[half * a.E + e] + s_agg[half * a.E + e] : 0;
-            int incl = v2;
-#pragma unroll
-            for (int d = 1; d < 32; d <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, incl, d);
-                if (lane >= d) incl += u;
-            }
-            if (e < a.E) {
-                off[e] = carry + incl - v2;
-                if (!half) a.tokens_per_expert[e] = v2;
-            }
-            carry += __shfl_sync(0xffffffffu, incl, 31);
-        }
-        if (lane == 0) off[a.E] = carry;
-    }
 }
 
-// The count / offset outputs written by the last scan tile are read back here
-// (stream order makes them visible).
+// Block-wide exclusive prefixes of the expert totals (the last tile's
+// inclusive count vector, E expert counts then E primary counts): every
+// finalize block computes them for itself, s_eoff[0..E] and s_poff[0..E].
+__device__ void expert_offsets(const int32_t* totals, int E, int32_t* s_eoff, int32_t* s_poff, int32_t* s_warp) {
+    constexpr int kWarps = kFinalizeThreads / 32;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int per = (E + kFinalizeThreads - 1) / kFinalizeThreads;     // <= 4 (E <= 1024)
+    const int b = tid * per;
+    int ve[4], vp[4];
+    int se = 0, sp = 0;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = b + u;
+        const bool in = u < per && e < E;
+        ve[u] = in ? __ldcg(totals + e) : 0;
+        vp[u] = in ? __ldcg(totals + E + e) : 0;
+        se += ve[u];
+        sp += vp[u];
+    }
+    int ie = se, ip = sp;                 // inclusive scans across the warp
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int ue = __shfl_up_sync(0xffffffffu, ie, d);
+        const int up = __shfl_up_sync(0xffffffffu, ip, d);
+        if (lane >= d) { ie += ue; ip += up; }
+    }
+    if (lane == 31) { s_warp[warp] = ie; s_warp[kWarps + warp] = ip; }
+    __syncthreads();
+    int be = ie - se, bp = ip - sp;       // exclusive within the warp
+    for (int w = 0; w < warp; ++w) { be += s_warp[w]; bp += s_warp[kWarps + w]; }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const int e = b + u;
+        if (u < per && e < E) { s_eoff[e] = be; s_poff[e] = bp; }
+        be += ve[u];
+        bp += vp[u];
+    }
+    if (tid == kFinalizeThreads - 1) { s_eoff[E] = be; s_poff[E] = bp; }
+    __syncthreads();
+}
+
+// The last scan tile's inclusive counts are read back here (stream order, or
+// the programmatic-launch wait, makes them visible).
 struct FinalArgs {
     const int32_t* topk_idx;
     const float* topk_w;
     int32_t T, K, E, R, m;
     int64_t capacity;
+    int32_t num_tiles;
     LayoutWs ws;
     uint32_t* status;
-    const int32_t *expert_offset, *recv_expert_offset;
+    int32_t *tokens_per_expert, *expert_offset, *recv_expert_offset;
     int32_t *tokens_per_rank, *rank_offset;
     int32_t *recv_slot, *expert_slot, *recv_src_token, *expert_src_row;
     float* expert_weight;
@@ -356,11 +385,10 @@ layout_finalize_kernel(FinalArgs a) {
 
     pdl_wait();
     pdl_trigger();          // one wave of CTAs: the dispatch grid may become resident now
-    for (int i = tid; i < E1; i += kFinalizeThreads) {
-        s_eoff[i] = a.expert_offset[i];
-        s_poff[i] = a.recv_expert_offset[i];
-        if (i < a.E) s_rank[i] = i / a.m;
-    }
+    __shared__ int32_t s_warp[2 * (kFinalizeThreads / 32)];
+    for (int i = tid; i < a.E; i += kFinalizeThreads) s_rank[i] = i / a.m;
+    const int32_t* totals = a.ws.tile_incl + static_cast<int64_t>(a.num_tiles - 1) * vec_width(a.E);
+    expert_offsets(totals, a.E, s_eoff, s_poff, s_warp);
     for (int i = tid; i < n; i += kFinalizeThreads) {
         int e = a.topk_idx[e0 + i];
         if (e < 0 || e >= a.E) e = -1;
@@ -419,6 +447,11 @@ layout_finalize_kernel(FinalArgs a) {
         a.expert_weight[i] = 0.0f;
     }
     if (blockIdx.x == 0) {
+        for (int e = tid; e <= a.E; e += kFinalizeThreads) {
+            a.expert_offset[e] = s_eoff[e];
+            a.recv_expert_offset[e] = s_poff[e];
+            if (e < a.E) a.tokens_per_expert[e] = s_eoff[e + 1] - s_eoff[e];
+        }
         for (int r = tid; r <= a.R; r += kFinalizeThreads) {
             a.rank_offset[r] = s_poff[r * a.m];
             if (r < a.R) a.tokens_per_rank[r] = s_poff[(r + 1) * a.m] - s_poff[r * a.m];
@@ -481,8 +514,6 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.T = L->T; sa.K = L->K; sa.E = L->E; sa.m = L->E / L->R; sa.R = L->R;
     sa.tile_tokens = L->tile_tokens; sa.num_tiles = L->num_tiles;
     sa.ws = ws; sa.status = L->status;
-    sa.tokens_per_expert = L->tokens_per_expert; sa.expert_offset = L->expert_offset;
-    sa.recv_expert_offset = L->recv_expert_offset;
     sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
     const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
                                             static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
@@ -495,7 +526,8 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     FinalArgs fa;
     fa.topk_idx = topk_idx; fa.topk_w = topk_w;
     fa.T = L->T; fa.K = L->K; fa.E = L->E; fa.R = L->R; fa.m = L->E / L->R;
-    fa.capacity = L->capacity; fa.ws = ws; fa.status = L->status;
+    fa.capacity = L->capacity; fa.num_tiles = L->num_tiles; fa.ws = ws; fa.status = L->status;
+    fa.tokens_per_expert = L->tokens_per_expert;
     fa.expert_offset = L->expert_offset; fa.recv_expert_offset = L->recv_expert_offset;
     fa.tokens_per_rank = L->tokens_per_rank; fa.rank_offset = L->rank_offset;
     fa.recv_slot = L->recv_slot; fa.expert_slot = L->expert_slot; fa.recv_src_token = L->recv_src_token;
