@@ -76,6 +76,25 @@ def committed_traffic(kernel_file: str, profile_name: str):
         return None
 
 
+# ------------------------------------------------------------- multi-rank
+
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """Slowest rank's time (replicas run in lock step between barriers)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_gbps(step_bytes: int, ms_step_max: float, world: int) -> float:
+    """Whole-job throughput: every replica moves step_bytes per step; the job
+    takes as long as its slowest rank."""
+    return world * step_bytes / (ms_step_max * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
@@ -232,10 +251,7 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     lay = [e[0].elapsed_time(e[1]) for e in ev_split]
     dis = [e[1].elapsed_time(e[2]) for e in ev_split]
-    if world > 1:
-        t = torch.tensor([ms_step], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_step = float(t.item())
+    ms_step = max_over_ranks(ms_step, world, dev)
 
     # FP8 dispatch, timed the same way (secondary figure)
     ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 3))]
@@ -255,7 +271,7 @@ def run_ours(args, rank, world, local_rank):
     gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
     result = {
         "metric": METRIC,
-        "value": round(world * step_bytes / (ms_step * 1e-3) / 1e9, 1),
+        "value": round(aggregate_gbps(step_bytes, ms_step, world), 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,

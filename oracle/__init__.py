@@ -50,26 +50,40 @@ _lib = None
 def lib() -> ctypes.CDLL:
     global _lib
     if _lib is None:
-        _lib = ctypes.CDLL(build())
-        P = ctypes.c_void_p
-        i32, i64 = ctypes.c_int32, ctypes.c_int64
-        _lib.moe_ref_bf16_encode.restype = ctypes.c_uint16
-        _lib.moe_ref_bf16_encode.argtypes = [ctypes.c_float]
-        _lib.moe_ref_bf16_decode.restype = ctypes.c_float
-        _lib.moe_ref_bf16_decode.argtypes = [ctypes.c_uint16]
-        _lib.moe_ref_e4m3_encode.restype = ctypes.c_uint8
-        _lib.moe_ref_e4m3_encode.argtypes = [ctypes.c_float]
-        _lib.moe_ref_e4m3_decode.restype = ctypes.c_float
-        _lib.moe_ref_e4m3_decode.argtypes = [ctypes.c_uint8]
-        _lib.moe_ref_layout.restype = ctypes.c_int
-        _lib.moe_ref_layout.argtypes = [P, P, i32, i32, i32, i32, i64] + [P] * 10
-        _lib.moe_ref_dispatch_bf16.restype = ctypes.c_int
-        _lib.moe_ref_dispatch_bf16.argtypes = [P, i32, i32, i32, P, i64, P]
-        _lib.moe_ref_dispatch_fp8.restype = ctypes.c_int
-        _lib.moe_ref_dispatch_fp8.argtypes = [P, i32, i32, i32, P, i64, P, P]
-        _lib.moe_ref_combine.restype = ctypes.c_int
-        _lib.moe_ref_combine.argtypes = [P, i64, i32, i32, i32, P, P, P]
+        _lib = load(build())
     return _lib
+
+
+def set_library(cdll: ctypes.CDLL | None) -> None:
+    """Route every oracle call to another build of moe_oracle.c (the mutation
+    tests use this to check that the pins catch planted mistakes); None
+    restores the default library."""
+    global _lib
+    _lib = cdll
+
+
+def load(path: str) -> ctypes.CDLL:
+    """Load a build of moe_oracle.c and declare its signatures."""
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    i32, i64 = ctypes.c_int32, ctypes.c_int64
+    L.moe_ref_bf16_encode.restype = ctypes.c_uint16
+    L.moe_ref_bf16_encode.argtypes = [ctypes.c_float]
+    L.moe_ref_bf16_decode.restype = ctypes.c_float
+    L.moe_ref_bf16_decode.argtypes = [ctypes.c_uint16]
+    L.moe_ref_e4m3_encode.restype = ctypes.c_uint8
+    L.moe_ref_e4m3_encode.argtypes = [ctypes.c_float]
+    L.moe_ref_e4m3_decode.restype = ctypes.c_float
+    L.moe_ref_e4m3_decode.argtypes = [ctypes.c_uint8]
+    L.moe_ref_layout.restype = ctypes.c_int
+    L.moe_ref_layout.argtypes = [P, P, i32, i32, i32, i32, i64] + [P] * 10
+    L.moe_ref_dispatch_bf16.restype = ctypes.c_int
+    L.moe_ref_dispatch_bf16.argtypes = [P, i32, i32, i32, P, i64, P]
+    L.moe_ref_dispatch_fp8.restype = ctypes.c_int
+    L.moe_ref_dispatch_fp8.argtypes = [P, i32, i32, i32, P, i64, P, P]
+    L.moe_ref_combine.restype = ctypes.c_int
+    L.moe_ref_combine.argtypes = [P, i64, i32, i32, i32, P, P, P]
+    return L
 
 
 def _ptr(a: np.ndarray | None):
