@@ -42,8 +42,10 @@ def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
     layout = 4 * T * K * 2 + 4 * T * R + 4 * T * K * 3 + 4 * capacity + 4 * (3 * E + 2 * R + 4)
     dispatch = 2 * T * H + 2 * H * n_pairs + 4 * T * R
     dispatch_fp8 = 2 * T * H + n_pairs * (H + 4 * (H // 128)) + 4 * T * R
+    dispatch_mxfp8 = 2 * T * H + n_pairs * (H + H // 32) + 4 * T * R
     combine = 2 * H * n_valid + 2 * T * H + 8 * T * K
-    return {"layout": layout, "dispatch": dispatch, "dispatch_fp8": dispatch_fp8, "combine": combine}
+    return {"layout": layout, "dispatch": dispatch, "dispatch_fp8": dispatch_fp8, "dispatch_mxfp8": dispatch_mxfp8,
+            "combine": combine}
 
 
 def measured_peaks():
@@ -186,7 +188,8 @@ def run_ours(args, rank, world, local_rank):
     w = inp.topk_w.to(dev)
     y = inp.y.to(dev)
     recv, _ = ep.alloc_recv(L, H, False, device=dev)
-    recv8, scales8 = ep.alloc_recv(L, H, True, device=dev)
+    recv8, scales8 = ep.alloc_recv(L, H, ep.MOE_FORMAT_FP8, device=dev)
+    recvmx, scalesmx = ep.alloc_recv(L, H, ep.MOE_FORMAT_MXFP8, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
@@ -258,10 +261,18 @@ def run_ours(args, rank, world, local_rank):
     for e in ev8:
         flush()
         e[0].record(stream)
-        ep.moe_dispatch(x, L, True, recv8, scales8, stream)
+        ep.moe_dispatch(x, L, ep.MOE_FORMAT_FP8, recv8, scales8, stream)
         e[1].record(stream)
     torch.cuda.synchronize(dev)
     dis8 = [e[0].elapsed_time(e[1]) for e in ev8]
+    evmx = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 3))]
+    for e in evmx:
+        flush()
+        e[0].record(stream)
+        ep.moe_dispatch(x, L, ep.MOE_FORMAT_MXFP8, recvmx, scalesmx, stream)
+        e[1].record(stream)
+    torch.cuda.synchronize(dev)
+    dismx = [e[0].elapsed_time(e[1]) for e in evmx]
 
     e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if rank == 0 else None
 
@@ -299,6 +310,9 @@ def run_ours(args, rank, world, local_rank):
             "dispatch_fp8": {"us": round(statistics.mean(dis8) * 1e3, 2), "bytes": ab["dispatch_fp8"],
                              "GB/s": round(gbps(ab["dispatch_fp8"], statistics.mean(dis8)), 1),
                              "frac": round(gbps(ab["dispatch_fp8"], statistics.mean(dis8)) / peak, 4)},
+            "dispatch_mxfp8": {"us": round(statistics.mean(dismx) * 1e3, 2), "bytes": ab["dispatch_mxfp8"],
+                               "GB/s": round(gbps(ab["dispatch_mxfp8"], statistics.mean(dismx)), 1),
+                               "frac": round(gbps(ab["dispatch_mxfp8"], statistics.mean(dismx)) / peak, 4)},
         },
         "roofline": {"bound": "hbm", "kernel": "combine_kernel<8>", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -121,13 +121,15 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w, int
                                         tuning ? tuning->debug_flags : 0u));
 }
 
-moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int fp8, void* recv_x,
-                        float* recv_scales, void* stream, const moe_tuning* tuning) {
+moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format, void* recv_x,
+                        void* recv_scales, void* stream, const moe_tuning* tuning) {
     if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (format != MOE_FORMAT_BF16 && format != MOE_FORMAT_FP8 && format != MOE_FORMAT_MXFP8) return MOE_ERR_INVALID_ARG;
     if (L->T > 0 && (!x || !recv_x)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(recv_x)) return MOE_ERR_INVALID_ARG;
-    if (fp8) {
-        if (hidden % 128 != 0 || !recv_scales || !aligned16(recv_scales)) return MOE_ERR_INVALID_ARG;
+    if (format != MOE_FORMAT_BF16) {
+        if (hidden % 128 != 0 || (L->T > 0 && !recv_scales) || (reinterpret_cast<uintptr_t>(recv_scales) & 3u) != 0)
+            return MOE_ERR_INVALID_ARG;
     } else if (recv_scales) {
         return MOE_ERR_INVALID_ARG;
     }
@@ -136,7 +138,7 @@ moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, 
                    (tuning->chunk_bytes != 0 && (tuning->chunk_bytes < 256 || tuning->chunk_bytes % 256 != 0)) ||
                    tuning->variant < 0 || tuning->variant > 2))
         return MOE_ERR_INVALID_ARG;
-    return from_cuda(moe::launch_dispatch(x, hidden, L, fp8 != 0, recv_x, recv_scales,
+    return from_cuda(moe::launch_dispatch(x, hidden, L, format, recv_x, recv_scales,
                                           static_cast<cudaStream_t>(stream), tuning ? tuning->num_channels : 0,
                                           tuning ? tuning->stages : 0, tuning ? tuning->chunk_bytes : 0,
                                           tuning ? tuning->variant : 0, timeout_of(tuning)));

@@ -37,7 +37,7 @@ constexpr int kFp8Threads = 256;
 struct DispatchArgs {
     const uint8_t* x;            // bf16 [T, H]
     uint8_t* recv;               // bf16 or E4M3 [capacity, H]
-    float* recv_scales;          // [capacity, H/128] (FP8 only)
+    uint32_t* recv_scales;       // [capacity, H/128] 32-bit scale words (FP8: fp32, MXFP8: 4 x E8M0)
     const int32_t* recv_slot;    // [T, R]
     int32_t T, H, R;
     int64_t capacity;
@@ -158,6 +158,10 @@ dispatch_bf16_kernel(DispatchArgs a) {
 // One item = one column chunk of one token.  A 128-column block is 256 bytes of
 // bf16: sixteen lanes hold 16 bytes each, so a warp quantises two blocks at a
 // time; the block amax is reduced across the half-warp.
+// FMT 1: FP8 with one fp32 scale per 1x128 block; FMT 2: MXFP8 with four
+// E8M0 bytes per 128 columns.  Either way one 32-bit scale word per 128-column
+// group goes to each destination row.
+template <int FMT>
 __global__ void __launch_bounds__(kFp8Threads)
 dispatch_fp8_kernel(DispatchArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -173,7 +177,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
     const int S = a.stages;
     const int nbc = a.chunk_elems / 128;                   // blocks per chunk
     const int nb_row = a.H / 128;
-    float* s_scale = reinterpret_cast<float*>(rest);       // [S][nbc]
+    uint32_t* s_scale = reinterpret_cast<uint32_t*>(rest);  // [S][nbc] scale words
     uint8_t* stage_in = rest + align_up(sizeof(float) * S * nbc, 128);
     const uint32_t in_bytes = static_cast<uint32_t>(a.chunk_elems) * 2u;
     uint8_t* stage_out = stage_in + static_cast<size_t>(S) * in_bytes;
@@ -235,11 +239,19 @@ dispatch_fp8_kernel(DispatchArgs a) {
                 va = *reinterpret_cast<const uint4*>(in + b * 256 + li * 16);
                 vb = *reinterpret_cast<const uint4*>(in + b * 256 + 128 + li * 16);
             }
-            const BlockQuant bq = quantize_block_share(va, vb);
+            uint2 q0, q1;
+            uint32_t word;
+            if constexpr (FMT == 1) {
+                const BlockQuant bq = quantize_block_share(va, vb);
+                q0 = bq.q0; q1 = bq.q1; word = __float_as_uint(bq.scale);
+            } else {
+                const MxQuant mq = quantize_group_share_mx(va, vb);
+                q0 = mq.q0; q1 = mq.q1; word = mq.scales;
+            }
             if (active) {
-                *reinterpret_cast<uint2*>(out + b * 128 + li * 8) = bq.q0;
-                *reinterpret_cast<uint2*>(out + b * 128 + 64 + li * 8) = bq.q1;
-                if (li == 0) s_scale[s * nbc + b] = bq.scale;
+                *reinterpret_cast<uint2*>(out + b * 128 + li * 8) = q0;
+                *reinterpret_cast<uint2*>(out + b * 128 + 64 + li * 8) = q1;
+                if (li == 0) s_scale[s * nbc + b] = word;
             }
         }
         fence_proxy_async_smem();
@@ -261,7 +273,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
             const int r = j / nb, b = j - r * nb;
             const int32_t slot = trow[r];
             if (slot < 0 || slot >= a.capacity) continue;
-            a.recv_scales[static_cast<int64_t>(slot) * nb_row + c * nbc + b] = s_scale[s * nbc + b];
+            a.recv_scales[static_cast<int64_t>(slot) * nb_row + c * nbc + b] = s_scale[s * nbc + b];   // 32-bit word
         }
     }
     pdl_trigger();
@@ -291,13 +303,14 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return v;
 }
 
-template <bool FP8>
+template <int FMT>
 __device__ __forceinline__ int lsu_col(int col0, int lane, int j) {
-    if constexpr (FP8) return col0 + (lane >> 3) * 128 + j * 64 + (lane & 7) * 8;
+    if constexpr (FMT != 0) return col0 + (lane >> 3) * 128 + j * 64 + (lane & 7) * 8;
     return col0 + j * 256 + lane * 8;
 }
 
-template <bool FP8>
+// FMT 0: bf16 rows; 1: FP8 with fp32 1x128 scales; 2: MXFP8 (E8M0 1x32 scales).
+template <int FMT>
 __global__ void __launch_bounds__(kLsuThreads)
 dispatch_lsu_kernel(DispatchArgs a) {
     pdl_wait();
@@ -325,7 +338,7 @@ dispatch_lsu_kernel(DispatchArgs a) {
             slot_lane[u] = (live[u] && lane < a.R) ? __ldg(a.recv_slot + t * a.R + lane) : -1;
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                const int col = lsu_col<FP8>(col0[u], lane, j);
+                const int col = lsu_col<FMT>(col0[u], lane, j);
                 v[u][j] = (live[u] && col < a.H) ? ld_nc_v4(a.x + (t * a.H + col) * 2) : make_uint4(0u, 0u, 0u, 0u);
             }
         }
@@ -333,8 +346,15 @@ dispatch_lsu_kernel(DispatchArgs a) {
         for (int u = 0; u < 2; ++u) {
             if (!live[u]) continue;
             const int64_t t = tok[u];
-            BlockQuant bq;
-            if constexpr (FP8) bq = quantize_block_share(v[u][0], v[u][1]);
+            uint2 q0 = make_uint2(0u, 0u), q1 = q0;
+            uint32_t word = 0;
+            if constexpr (FMT == 1) {
+                const BlockQuant bq = quantize_block_share(v[u][0], v[u][1]);
+                q0 = bq.q0; q1 = bq.q1; word = __float_as_uint(bq.scale);
+            } else if constexpr (FMT == 2) {
+                const MxQuant mq = quantize_group_share_mx(v[u][0], v[u][1]);
+                q0 = mq.q0; q1 = mq.q1; word = mq.scales;
+            }
             for (int rbase = 0; rbase < a.R; rbase += 32) {
                 const int32_t my_slot = rbase == 0 ? slot_lane[u]
                                                    : (lane + rbase < a.R ? __ldg(a.recv_slot + t * a.R + rbase + lane) : -1);
@@ -345,12 +365,12 @@ dispatch_lsu_kernel(DispatchArgs a) {
                     if (slot >= a.capacity) { bad = true; continue; }
 #pragma unroll
                     for (int j = 0; j < 2; ++j) {
-                        const int col = lsu_col<FP8>(col0[u], lane, j);
+                        const int col = lsu_col<FMT>(col0[u], lane, j);
                         if (col >= a.H) continue;
-                        if constexpr (FP8) {
-                            *reinterpret_cast<uint2*>(a.recv + static_cast<int64_t>(slot) * a.H + col) = j ? bq.q1 : bq.q0;
+                        if constexpr (FMT != 0) {
+                            *reinterpret_cast<uint2*>(a.recv + static_cast<int64_t>(slot) * a.H + col) = j ? q1 : q0;
                             if (j == 0 && (lane & 7) == 0)
-                                a.recv_scales[static_cast<int64_t>(slot) * nb_row + col / 128] = bq.scale;
+                                a.recv_scales[static_cast<int64_t>(slot) * nb_row + col / 128] = word;
                         } else {
                             *reinterpret_cast<uint4*>(a.recv + (static_cast<int64_t>(slot) * a.H + col) * 2) = v[u][j];
                         }
@@ -365,16 +385,17 @@ dispatch_lsu_kernel(DispatchArgs a) {
 
 }  // namespace
 
-cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
-                            void* recv_x, float* recv_scales, cudaStream_t stream,
+cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
+                            void* recv_x, void* recv_scales, cudaStream_t stream,
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
                             uint64_t timeout_ns) {
     if (L->T == 0) return cudaSuccess;
     DispatchArgs a;
     a.x = reinterpret_cast<const uint8_t*>(x);
     a.recv = static_cast<uint8_t*>(recv_x);
-    a.recv_scales = recv_scales;
+    a.recv_scales = static_cast<uint32_t*>(recv_scales);
     a.recv_slot = L->recv_slot;
+    const bool fp8 = format != MOE_FORMAT_BF16;
     a.T = L->T; a.H = hidden; a.R = L->R;
     a.capacity = L->capacity;
     a.status = L->status;
@@ -410,8 +431,9 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     }
     if (variant == 2) {
         // 16-byte vector path: persistent grid, occupancy-limited
-        const void* fn = fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<true>)
-                             : reinterpret_cast<const void*>(dispatch_lsu_kernel<false>);
+        const void* fn = format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2>)
+                         : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1>)
+                               : reinterpret_cast<const void*>(dispatch_lsu_kernel<0>);
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLsuThreads, 0);
         if (e != cudaSuccess) return e;
@@ -422,19 +444,21 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
         const int64_t need = (warps_needed * 32 + kLsuThreads - 1) / kLsuThreads;
         if (lsu_grid > need) lsu_grid = need;
         if (lsu_grid < 1) lsu_grid = 1;
-        if (fp8)
-            return launch_pdl(dispatch_lsu_kernel<true>, dim3(static_cast<unsigned>(lsu_grid)), dim3(kLsuThreads), 0,
-                              stream, a);
-        return launch_pdl(dispatch_lsu_kernel<false>, dim3(static_cast<unsigned>(lsu_grid)), dim3(kLsuThreads), 0,
-                          stream, a);
+        const dim3 g(static_cast<unsigned>(lsu_grid)), b(kLsuThreads);
+        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2>, g, b, 0, stream, a);
+        if (fp8) return launch_pdl(dispatch_lsu_kernel<1>, g, b, 0, stream, a);
+        return launch_pdl(dispatch_lsu_kernel<0>, g, b, 0, stream, a);
     }
-    const void* fn = fp8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel)
-                         : reinterpret_cast<const void*>(dispatch_bf16_kernel);
+    const void* fn = format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel<2>)
+                     : fp8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel<1>)
+                           : reinterpret_cast<const void*>(dispatch_bf16_kernel);
     const int threads = fp8 ? kFp8Threads : 32;
     cudaError_t err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (err != cudaSuccess) return err;
     if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
-    if (fp8) return launch_pdl(dispatch_fp8_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, a);
+    if (format == MOE_FORMAT_MXFP8)
+        return launch_pdl(dispatch_fp8_kernel<2>, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, a);
+    if (fp8) return launch_pdl(dispatch_fp8_kernel<1>, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, a);
     return launch_pdl(dispatch_bf16_kernel, dim3(static_cast<unsigned>(grid)), dim3(threads), smem, stream, a);
 }
 

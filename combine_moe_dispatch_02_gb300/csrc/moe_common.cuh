@@ -220,8 +220,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 namespace moe {
 cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const moe_layout* L,
                           cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags);
-cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, bool fp8,
-                            void* recv_x, float* recv_scales, cudaStream_t stream,
+cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
+                            void* recv_x, void* recv_scales, cudaStream_t stream,
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
                             uint64_t timeout_ns);
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,

@@ -34,6 +34,10 @@ MOE_DEVERR_TIMEOUT = 0x4
 
 MOE_DEBUG_STALL_FIRST_TILE = 0x1
 
+MOE_FORMAT_BF16 = 0
+MOE_FORMAT_FP8 = 1
+MOE_FORMAT_MXFP8 = 2
+
 EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
             "moe_dispatch", "moe_combine", "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
 
@@ -88,7 +92,7 @@ def lib() -> ctypes.CDLL:
         L.moe_dispatch_layout_noalloc.argtypes = [P, P, i32, i32, ctypes.POINTER(moe_layout), P,
                                                   ctypes.POINTER(moe_tuning)]
         L.moe_dispatch.restype = ctypes.c_int
-        L.moe_dispatch.argtypes = [P, i32, ctypes.POINTER(moe_layout), ctypes.c_int, P, P, P,
+        L.moe_dispatch.argtypes = [P, i32, ctypes.POINTER(moe_layout), i32, P, P, P,
                                    ctypes.POINTER(moe_tuning)]
         L.moe_combine.restype = ctypes.c_int
         L.moe_combine.argtypes = [P, i32, ctypes.POINTER(moe_layout), P, P, P, ctypes.POINTER(moe_tuning)]
@@ -200,11 +204,13 @@ def moe_dispatch_layout_noalloc(topk_idx: torch.Tensor, topk_w: torch.Tensor | N
                                              _stream(stream), _tuning(**tuning)), "moe_dispatch_layout_noalloc")
 
 
-def moe_dispatch(x: torch.Tensor, L: Layout, fp8: bool, recv_x: torch.Tensor,
+def moe_dispatch(x: torch.Tensor, L: Layout, fmt, recv_x: torch.Tensor,
                  recv_scales: torch.Tensor | None = None, stream=None, **tuning) -> None:
+    """fmt: MOE_FORMAT_BF16 / MOE_FORMAT_FP8 / MOE_FORMAT_MXFP8 (False / True
+    stand for bf16 / FP8)."""
     assert x.dtype == torch.bfloat16 and x.is_contiguous()
     assert recv_x.is_contiguous() and (recv_scales is None or recv_scales.is_contiguous())
-    _check(lib().moe_dispatch(_ptr(x), x.shape[-1], ctypes.byref(L.c), int(bool(fp8)), _ptr(recv_x),
+    _check(lib().moe_dispatch(_ptr(x), x.shape[-1], ctypes.byref(L.c), int(fmt), _ptr(recv_x),
                               _ptr(recv_scales), _stream(stream), _tuning(**tuning)), "moe_dispatch")
 
 
@@ -229,9 +235,13 @@ def moe_device_sm_count() -> int:
 
 # ------------------------------------------------------------ conveniences
 
-def alloc_recv(L: Layout, hidden: int, fp8: bool, device="cuda"):
+def alloc_recv(L: Layout, hidden: int, fmt, device="cuda"):
     """Receive buffers for moe_dispatch: (recv_x, recv_scales or None)."""
-    if fp8:
+    fmt = int(fmt)
+    if fmt == MOE_FORMAT_FP8:
         return (torch.empty(L.capacity, hidden, dtype=torch.uint8, device=device),
                 torch.empty(L.capacity, hidden // 128, dtype=torch.float32, device=device))
+    if fmt == MOE_FORMAT_MXFP8:
+        return (torch.empty(L.capacity, hidden, dtype=torch.uint8, device=device),
+                torch.empty(L.capacity, hidden // 32, dtype=torch.uint8, device=device))
     return torch.empty(L.capacity, hidden, dtype=torch.bfloat16, device=device), None

@@ -175,24 +175,36 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, const float* top
                                        int32_t num_experts, int32_t num_ranks,
                                        moe_layout* L, void* stream, const moe_tuning* tuning);
 
+/* Receive formats of moe_dispatch. */
+#define MOE_FORMAT_BF16  0   /* bf16 rows                                              */
+#define MOE_FORMAT_FP8   1   /* E4M3 rows + one fp32 scale per 1x128 block             */
+#define MOE_FORMAT_MXFP8 2   /* E4M3 rows + one E8M0 byte per 1x32 block (OCP MX)      */
+
 /* Dispatch: for every pair with recv_slot[t,r] >= 0 write token t's row into
  * receive row recv_slot[t,r]: each token once per destination rank, rows in
  * expert-contiguous order.
- *   fp8 == 0: recv_x is bf16 [capacity, hidden]; recv_scales must be NULL.
- *   fp8 != 0: recv_x is E4M3 bytes [capacity, hidden] and recv_scales fp32
- *     [capacity, hidden/128]: per token and 1x128 block, s = amax / 448 (fp32,
- *     round to nearest), q = E4M3(x / s) with round-to-nearest-even and
+ *   MOE_FORMAT_BF16: recv_x is bf16 [capacity, hidden]; recv_scales must be NULL.
+ *   MOE_FORMAT_FP8: recv_x is E4M3 bytes [capacity, hidden] and recv_scales
+ *     fp32 [capacity, hidden/128]: per token and 1x128 block, s = amax / 448
+ *     (fp32, round to nearest), q = E4M3(x / s) with round-to-nearest-even and
  *     saturation; an all-zero block gives s = 0 and q = 0.  FP8 dispatch:
  *     "MoE / Hybrid-EP Validation", "FP8 dispatch restriction"; the pages give
  *     no recipe, this one is the DeepEP-style 1x128 block scaling.
- * x is bf16 [T, hidden]; hidden % 8 == 0 (hidden % 128 == 0 for fp8); x,
- * recv_x, recv_scales 16-byte aligned.  Rows past rank_offset[R] are not
- * written.  Each CTA is an independent channel over a contiguous chunk of
- * tokens: TMA bulk loads of the row into shared memory, then one TMA bulk
- * store per destination row; no grid-wide synchronisation (Hybrid-EP news
- * article, "Technical Structure": each CUDA block an independent channel). */
-moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int fp8,
-                        void* recv_x, float* recv_scales, void* stream, const moe_tuning* tuning);
+ *   MOE_FORMAT_MXFP8: recv_x is E4M3 bytes [capacity, hidden] and recv_scales
+ *     E8M0 bytes [capacity, hidden/32] (OCP Microscaling MXFP8, the format of
+ *     the MXFP8 training on the Hybrid-EP news article, "Efficiency
+ *     Numbers"): per 1x32 block se = floor(log2(amax)) - 8 clamped to
+ *     [-127, 127] (-127 for an all-zero block), byte = se + 127,
+ *     q = E4M3(x * 2^-se), round to nearest even, saturating at 448.
+ * x is bf16 [T, hidden]; hidden % 8 == 0 (hidden % 128 == 0 for both FP8
+ * formats); x, recv_x 16-byte aligned, recv_scales 4-byte aligned.  Rows
+ * past rank_offset[R] are not written.  Each CTA is an independent channel
+ * over a contiguous chunk of tokens: TMA bulk loads of the row into shared
+ * memory, then one TMA bulk store per destination row; no grid-wide
+ * synchronisation (Hybrid-EP news article, "Technical Structure": each CUDA
+ * block an independent channel). */
+moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
+                        void* recv_x, void* recv_scales, void* stream, const moe_tuning* tuning);
 
 /* Combine: out[t,:] = bf16_rne( sum over k = 0..K-1 with expert_slot[t,k] >= 0
  * of topk_w[t,k] * y[expert_slot[t,k], :] ), accumulated in fp32 as a fused

@@ -81,6 +81,8 @@ def load(path: str) -> ctypes.CDLL:
     L.moe_ref_dispatch_bf16.argtypes = [P, i32, i32, i32, P, i64, P]
     L.moe_ref_dispatch_fp8.restype = ctypes.c_int
     L.moe_ref_dispatch_fp8.argtypes = [P, i32, i32, i32, P, i64, P, P]
+    L.moe_ref_dispatch_mxfp8.restype = ctypes.c_int
+    L.moe_ref_dispatch_mxfp8.argtypes = [P, i32, i32, i32, P, i64, P, P]
     L.moe_ref_combine.restype = ctypes.c_int
     L.moe_ref_combine.argtypes = [P, i64, i32, i32, i32, P, P, P]
     return L
@@ -185,6 +187,17 @@ def dispatch_fp8(x_bits: np.ndarray, L: Layout):
     recv_s = np.zeros((L.capacity, max(H // 128, 1)), np.float32)
     st = lib().moe_ref_dispatch_fp8(_ptr(x_bits), T, H, L.R, _ptr(L.recv_slot), L.capacity,
                                     _ptr(recv_q), _ptr(recv_s))
+    return recv_q, recv_s, st
+
+
+def dispatch_mxfp8(x_bits: np.ndarray, L: Layout):
+    """Returns (recv_q uint8 [capacity,H], recv_scales uint8 E8M0 [capacity,H/32], status)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    T, H = x_bits.shape
+    recv_q = np.zeros((L.capacity, H), np.uint8)
+    recv_s = np.zeros((L.capacity, max(H // 32, 1)), np.uint8)
+    st = lib().moe_ref_dispatch_mxfp8(_ptr(x_bits), T, H, L.R, _ptr(L.recv_slot), L.capacity,
+                                      _ptr(recv_q), _ptr(recv_s))
     return recv_q, recv_s, st
 
 

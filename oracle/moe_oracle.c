@@ -235,6 +235,53 @@ int moe_ref_dispatch_fp8(const uint16_t* x, int32_t T, int32_t H, int32_t R,
     return err;
 }
 
+/* OCP Microscaling (MX) formats: a block of 32 values shares one power-of-two
+ * scale X = 2^shared_exp stored as an E8M0 byte (biased exponent, bias 127);
+ * shared_exp is floor(log2 of the block's largest magnitude) minus the
+ * exponent of the element format's largest normal (8 for E4M3), so the
+ * largest element lands in [256, 512) before the element conversion, which
+ * rounds to nearest even and saturates at 448.  Multiplying by a power of two
+ * is exact except for results below the fp32 normal range, which ldexpf
+ * rounds once. */
+int moe_ref_dispatch_mxfp8(const uint16_t* x, int32_t T, int32_t H, int32_t R,
+                           const int32_t* recv_slot, int64_t capacity,
+                           uint8_t* recv_q, uint8_t* recv_scales)
+{
+    if (!x || !recv_slot || !recv_q || !recv_scales || T < 0 || H <= 0 || R <= 0 || H % 32 != 0)
+        return MOE_REF_ERR_ARG;
+    const int32_t nb = H / 32;
+    int err = 0;
+    uint8_t q_row[32];
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t b = 0; b < nb; ++b) {
+            float amax = 0.0f;
+            for (int32_t j = 0; j < 32; ++j) {
+                float v = fabsf(moe_ref_bf16_decode(x[t * H + b * 32 + j]));
+                if (v > amax) amax = v;
+            }
+            int shared_exp = -127;
+            if (amax > 0.0f) {
+                int e2;
+                frexpf(amax, &e2);                 /* amax = f * 2^e2, f in [0.5, 1) */
+                shared_exp = (e2 - 1) - 8;         /* floor(log2(amax)) - 8 */
+                if (shared_exp < -127) shared_exp = -127;
+                if (shared_exp > 127) shared_exp = 127;
+            }
+            for (int32_t j = 0; j < 32; ++j) {
+                float v = moe_ref_bf16_decode(x[t * H + b * 32 + j]);
+                q_row[j] = moe_ref_e4m3_encode(ldexpf(v, -shared_exp));
+            }
+            for (int32_t r = 0; r < R; ++r) {
+                int64_t slot = recv_slot[t * R + r];
+                if (slot < 0) continue;
+                if (slot >= capacity) { err |= MOE_REF_ERR_CAPACITY; continue; }
+                memcpy(recv_q + slot * H + (int64_t)b * 32, q_row, 32);
+                recv_scales[slot * nb + b] = (uint8_t)(shared_exp + 127);
+            }
+        }
+    return err;
+}
+
 /* --------------------------------------------------------------- combine */
 
 int moe_ref_combine(const uint16_t* y, int64_t n_rows, int32_t T, int32_t K,

@@ -88,6 +88,16 @@ int moe_ref_dispatch_fp8(const uint16_t* x, int32_t T, int32_t H, int32_t R,
                          const int32_t* recv_slot, int64_t capacity,
                          uint8_t* recv_q, float* recv_scales);
 
+/* MXFP8 dispatch (OCP Microscaling, E4M3 elements, E8M0 shared scale):
+ * per token and 1x32 block, shared_exp = floor(log2(amax)) - 8 (8 is the
+ * exponent of E4M3's largest normal, 448 = 1.75 * 2^8), clamped to
+ * [-127, 127]; an all-zero block takes -127.  Scale byte = shared_exp + 127;
+ * q = E4M3_RNE_satfinite(x * 2^-shared_exp).  H % 32 == 0.
+ * recv_q [capacity,H] bytes, recv_scales [capacity,H/32] bytes. */
+int moe_ref_dispatch_mxfp8(const uint16_t* x, int32_t T, int32_t H, int32_t R,
+                           const int32_t* recv_slot, int64_t capacity,
+                           uint8_t* recv_q, uint8_t* recv_scales);
+
 /* Combine: out[t,:] = bf16_rne( fp32 fma chain over k ascending of
  * topk_w[t,k] * y[expert_slot[t,k], :] ), skipping expert_slot < 0.
  * y [n_rows,H] bf16 bits (expert-major), out [T,H] bf16 bits. */

@@ -15,7 +15,8 @@ LAYOUT_FIELDS = ("tokens_per_expert", "expert_offset", "tokens_per_rank", "rank_
 
 
 def gpu_run(x, topk_idx, topk_w, y, E, R, fp8=False, capacity=None, reps=1, **tuning):
-    """Layout -> dispatch -> combine on cuda:0.  Returns numpy copies of every
+    """Layout -> dispatch -> combine on cuda:0.  `fp8` is a receive format
+    (False/0 bf16, True/1 FP8 1x128, 2 MXFP8).  Returns numpy copies of every
     output, the receive buffers and the status."""
     dev = torch.device("cuda", 0)
     T, K = topk_idx.shape
@@ -37,7 +38,7 @@ def gpu_run(x, topk_idx, topk_w, y, E, R, fp8=False, capacity=None, reps=1, **tu
     n_pairs = int(res["rank_offset"][R])
     if fp8:
         res["recv_q"] = recv_x[:n_pairs].cpu().numpy()
-        res["recv_scales"] = recv_s[:n_pairs].cpu().numpy()
+        res["recv_scales"] = recv_s[:n_pairs].cpu().numpy().copy()
     else:
         res["recv_x"] = bf16_bits(recv_x[:n_pairs].cpu())
     if y is not None:
@@ -54,7 +55,10 @@ def oracle_run(x, topk_idx, topk_w, y, E, R, fp8=False, capacity=None):
     res = {f: getattr(L, f) for f in LAYOUT_FIELDS}
     xb = bf16_bits(x)
     n_pairs = L.n_pairs
-    if fp8:
+    if int(fp8) == 2:
+        q, s, st = oracle.dispatch_mxfp8(xb, L)
+        res["recv_q"], res["recv_scales"] = q[:n_pairs], s[:n_pairs]
+    elif fp8:
         q, s, st = oracle.dispatch_fp8(xb, L)
         res["recv_q"], res["recv_scales"] = q[:n_pairs], s[:n_pairs]
     else:
@@ -83,7 +87,8 @@ def assert_parity(g, o, fp8=False, combine_ulps=1):
     assert g["n_pairs"] == o["n_pairs"]
     if fp8:
         assert np.array_equal(g["recv_q"], o["recv_q"]), "FP8 codes differ"
-        assert np.array_equal(g["recv_scales"].view(np.uint32), o["recv_scales"].view(np.uint32)), "FP8 scales differ"
+        gs, os_ = np.ascontiguousarray(g["recv_scales"]), np.ascontiguousarray(o["recv_scales"])
+        assert gs.dtype == os_.dtype and np.array_equal(gs.view(np.uint8), os_.view(np.uint8)), "FP8 scales differ"
     else:
         assert np.array_equal(g["recv_x"], o["recv_x"]), "bf16 receive rows differ"
     if "out" in o:

@@ -70,6 +70,9 @@ def test_operator_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.moe_dispatch(ctypes.c_void_p((1 << 21) + 2), 64, ctypes.byref(L), 0, p, None, None, None) \
         == ep.MOE_ERR_INVALID_ARG
     assert lib.moe_dispatch(p, 64, ctypes.byref(L), 1, p, p, None, None) == ep.MOE_ERR_INVALID_ARG
+    assert lib.moe_dispatch(p, 64, ctypes.byref(L), 2, p, p, None, None) == ep.MOE_ERR_INVALID_ARG   # MXFP8 needs hidden % 128
+    assert lib.moe_dispatch(p, 128, ctypes.byref(L), 3, p, p, None, None) == ep.MOE_ERR_INVALID_ARG  # no such format
+    assert lib.moe_dispatch(p, 128, ctypes.byref(L), 2, p, None, None, None) == ep.MOE_ERR_INVALID_ARG  # scales missing
     assert lib.moe_combine(p, 12, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
     assert lib.moe_combine(None, 64, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
 

@@ -250,3 +250,102 @@ def test_dispatch_identity_combine_returns_x(oracle_lib, name):
     out, st = oracle_lib.combine(y, L.expert_slot, inp.topk_w.numpy())
     assert st == 0
     assert np.array_equal(out, x)
+
+
+# ---------------------------------------------------------------- MXFP8 dispatch
+
+def _read_mx_golden():
+    import os
+    rows = []
+    with open(os.path.join(os.path.dirname(__file__), "golden", "mxfp8_values.txt")) as f:
+        for line in f:
+            line = line.split("#")[0].strip()
+            if line:
+                p = line.split()
+                rows.append((float(p[0]), int(p[1]), int(p[2]), float(p[3]), int(p[4], 16)))
+    return rows
+
+
+def _bf16_bits_of(v: float) -> int:
+    return int(torch.tensor([v], dtype=torch.float32).to(torch.bfloat16).view(torch.int16).item()) & 0xFFFF
+
+
+def test_mxfp8_golden_values(oracle_lib):
+    """Each golden line becomes one 32-value block: amax at column 0 (as +amax),
+    x at column 1, zeros elsewhere (a zero-amax line: an all-zero block)."""
+    rows = _read_mx_golden()
+    T, H = len(rows), 32
+    x = np.zeros((T, H), np.uint16)
+    for t, (amax, _, _, xv, _) in enumerate(rows):
+        x[t, 0] = _bf16_bits_of(amax)
+        x[t, 1] = _bf16_bits_of(xv)
+        assert float(torch.tensor([xv]).to(torch.bfloat16)) == xv      # fixtures are bf16 values
+    idx = np.arange(T, dtype=np.int32).reshape(T, 1) % 4
+    L = oracle_lib.layout(idx, None, 4, 4)
+    q, s, st = oracle_lib.dispatch_mxfp8(x, L)
+    assert st == 0
+    for t, (amax, se, byte, xv, code) in enumerate(rows):
+        slot = L.recv_slot[t][L.recv_slot[t] >= 0][0]
+        assert s[slot, 0] == byte == se + 127, (t, s[slot, 0], byte)
+        assert q[slot, 1] == code, (t, hex(q[slot, 1]), hex(code))
+
+
+def _exact_mx_block(xb):
+    """From the OCP MX definition, exactly: s = floor(log2 amax) - 8 (clamped), q = E4M3(RN32(x * 2^-s))."""
+    import math
+    vals = [bf16_value(int(b)) for b in xb]
+    amax = max(abs(v) for v in vals)
+    if amax == 0:
+        s = -127
+    else:
+        s = math.floor(math.log2(amax))
+        while Fraction(2) ** s > amax:          # guard the float log2
+            s -= 1
+        while Fraction(2) ** (s + 1) <= amax:
+            s += 1
+        s = min(max(s - 8, -127), 127)
+    return [rn_e4m3_sat(rn_f32(v * Fraction(2) ** (-s))) for v in vals], s
+
+
+def test_mxfp8_vs_exact_pipeline(oracle_lib):
+    T, H, E, R, K = 6, 128, 8, 2, 2
+    idx = random_routing(T, K, E, 12).numpy()
+    L = oracle_lib.layout(idx, None, E, R)
+    x = _x_bits(T, H, 17, scale=4.0)
+    x[0, 32:64] = 0                                   # zero block
+    x[1, :32] = _x_bits(1, 32, 3, scale=1e-36)[0]     # tiny (subnormal-range) block
+    x[2, 70] = 0x8000                                 # negative zero in a live block
+    q, s, st = oracle_lib.dispatch_mxfp8(x, L)
+    assert st == 0
+    table = _torch_e4m3_table()
+    for t in range(T):
+        for b in range(H // 32):
+            want_q, want_s = _exact_mx_block(x[t, b * 32:(b + 1) * 32])
+            for slot in L.recv_slot[t][L.recv_slot[t] >= 0]:
+                assert int(s[slot, b]) == want_s + 127, (t, b)
+                got = [Fraction(float(table[c])) for c in q[slot, b * 32:(b + 1) * 32]]
+                assert got == want_q, (t, b)
+    z = L.recv_slot[2][L.recv_slot[2] >= 0]
+    assert np.all(q[z, 70] == 0x80)
+
+
+def test_mxfp8_vs_library_pipeline(oracle_lib):
+    """torch's float8_e8m0fnu decodes the scale bytes, numpy multiplies by the
+    power of two, torch's float8_e4m3fn converts; on a DeepSeek-V3 slice."""
+    if not hasattr(torch, "float8_e8m0fnu"):
+        pytest.skip("torch without float8_e8m0fnu")
+    T, H, E, R = 32, 7168, 256, 8
+    inp = make_inputs(WORKLOADS["dsv3"].scaled(T), with_y=False)
+    L = oracle_lib.layout(inp.topk_idx.numpy(), None, E, R)
+    q, s, st = oracle_lib.dispatch_mxfp8(bf16_bits(inp.x), L)
+    assert st == 0
+    xf = inp.x.float().numpy().reshape(T, H // 32, 32)
+    amax = np.abs(xf).max(axis=2)
+    for t in range(T):
+        slot = L.recv_slot[t][L.recv_slot[t] >= 0][0]
+        scale = torch.from_numpy(s[slot].copy()).view(torch.float8_e8m0fnu).float().numpy()
+        # the scale puts the block max in [256, 512)
+        assert np.all((amax[t] / scale >= 256) & (amax[t] / scale < 512))
+        v = np.clip((xf[t] / scale[:, None]).astype(np.float32), -448, 448)
+        ref = torch.from_numpy(v.reshape(H)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        assert np.array_equal(q[slot], ref)

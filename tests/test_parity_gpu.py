@@ -166,3 +166,34 @@ def test_over_provisioned_capacity():
     g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, capacity=cap)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, capacity=cap)
     assert_parity(g, o)
+
+
+# ---------------------------------------------------------------- MXFP8 dispatch
+
+@pytest.mark.parametrize("name", ["dsv3", "qwen_skew", "ds16_wide"])
+def test_mxfp8_parity_full_size(name):
+    wl = WORKLOADS[name]
+    inp = make_inputs(wl, with_y=False)
+    o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=2)
+    for variant in (1, 2):
+        g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=2, variant=variant)
+        assert g["status"] == 0
+        assert_parity(g, o, fp8=True)
+
+
+@pytest.mark.parametrize("T,H,E,R,K,seed", [(1, 128, 4, 2, 2, 0), (333, 384, 32, 8, 6, 1), (128, 9216, 16, 4, 4, 2)])
+@pytest.mark.parametrize("variant", [1, 2])
+def test_mxfp8_edge_cases(T, H, E, R, K, seed, variant):
+    idx = random_routing(T, K, E, seed, mask_frac=0.1)
+    g_ = torch.Generator().manual_seed(seed + 5)
+    x = torch.randn(T, H, generator=g_) * 3
+    x[0, :32] = 0.0                                           # zero MX block
+    x[0, 32:64] = -0.0                                        # negative zeros: codes 0x80
+    if T > 1:
+        x[1, :32] = torch.randn(32, generator=g_) * 1e-38     # bf16 subnormal-range block
+        x[1, 64] = 3.3e38                                     # near the bf16 maximum
+    x = x.to(torch.bfloat16)
+    g = gpu_run(x, idx, None, None, E, R, fp8=2, variant=variant)
+    o = oracle_run(x, idx, None, None, E, R, fp8=2)
+    assert g["status"] == 0
+    assert_parity(g, o, fp8=True)
