@@ -44,7 +44,9 @@ def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
     dispatch_fp8 = 2 * T * H + n_pairs * (H + 4 * (H // 128)) + 4 * T * R
     dispatch_mxfp8 = 2 * T * H + n_pairs * (H + H // 32) + 4 * T * R
     combine = 2 * H * n_valid + 2 * T * H + 8 * T * K
-    return {"layout": layout, "dispatch": dispatch, "dispatch_fp8": dispatch_fp8, "dispatch_mxfp8": dispatch_mxfp8,
+    dispatch_bwd = 2 * H * n_pairs + 2 * T * H + 4 * T * R
+    combine_bwd = 2 * T * H + 4 * H * n_valid + 12 * T * K
+    return {"dispatch_backward": dispatch_bwd, "combine_backward": combine_bwd, "layout": layout, "dispatch": dispatch, "dispatch_fp8": dispatch_fp8, "dispatch_mxfp8": dispatch_mxfp8,
             "combine": combine}
 
 
@@ -274,6 +276,27 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize(dev)
     dismx = [e[0].elapsed_time(e[1]) for e in evmx]
 
+    # backward pair (secondary figures): gradients of the receive rows and of the output
+    grad_recv = torch.empty_like(recv).normal_()
+    grad_out = torch.empty_like(out).normal_()
+    grad_x = torch.empty_like(x)
+    grad_y = torch.empty_like(y)
+    grad_w = torch.empty_like(w)
+    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(args.steps // 4, 3))]
+    for e in evb:
+        flush()
+        e[0].record(stream)
+        ep.moe_dispatch_backward(grad_recv, L, grad_x, stream)
+        e[1].record(stream)
+        ep.moe_combine_backward(grad_out, y, L, w, grad_y, grad_w, stream)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    dbwd = [e[0].elapsed_time(e[1]) for e in evb]
+    cbwd = [e[1].elapsed_time(e[2]) for e in evb]
+    st, flags = ep.moe_layout_read_status(L, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after the secondary legs")
+
     e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if rank == 0 else None
 
     peak, peak_kind = measured_peaks()
@@ -313,6 +336,12 @@ def run_ours(args, rank, world, local_rank):
             "dispatch_mxfp8": {"us": round(statistics.mean(dismx) * 1e3, 2), "bytes": ab["dispatch_mxfp8"],
                                "GB/s": round(gbps(ab["dispatch_mxfp8"], statistics.mean(dismx)), 1),
                                "frac": round(gbps(ab["dispatch_mxfp8"], statistics.mean(dismx)) / peak, 4)},
+            "dispatch_backward": {"us": round(statistics.mean(dbwd) * 1e3, 2), "bytes": ab["dispatch_backward"],
+                                  "GB/s": round(gbps(ab["dispatch_backward"], statistics.mean(dbwd)), 1),
+                                  "frac": round(gbps(ab["dispatch_backward"], statistics.mean(dbwd)) / peak, 4)},
+            "combine_backward": {"us": round(statistics.mean(cbwd) * 1e3, 2), "bytes": ab["combine_backward"],
+                                 "GB/s": round(gbps(ab["combine_backward"], statistics.mean(cbwd)), 1),
+                                 "frac": round(gbps(ab["combine_backward"], statistics.mean(cbwd)) / peak, 4)},
         },
         "roofline": {"bound": "hbm", "kernel": "combine_kernel<8>", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -155,6 +155,29 @@ moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, c
                                          timeout_of(tuning)));
 }
 
+moe_status moe_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, const moe_layout* L, uint16_t* grad_x,
+                                 void* stream, const moe_tuning* tuning) {
+    if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (L->T > 0 && (!grad_recv || !grad_x)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(grad_recv) || !aligned16(grad_x)) return MOE_ERR_INVALID_ARG;
+    if (tuning && tuning->num_channels < 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_dispatch_backward(grad_recv, hidden, L, grad_x, static_cast<cudaStream_t>(stream),
+                                                   tuning ? tuning->num_channels : 0));
+}
+
+moe_status moe_combine_backward(const uint16_t* grad_out, const uint16_t* y, int32_t hidden, const moe_layout* L,
+                                const float* topk_w, uint16_t* grad_y, float* grad_w, void* stream,
+                                const moe_tuning* tuning) {
+    if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
+    if (L->T > 0 && (!grad_out || !y || !topk_w || !grad_y || !grad_w)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(grad_out) || !aligned16(y) || !aligned16(grad_y) ||
+        (reinterpret_cast<uintptr_t>(topk_w) & 3u) != 0 || (reinterpret_cast<uintptr_t>(grad_w) & 3u) != 0)
+        return MOE_ERR_INVALID_ARG;
+    if (tuning && tuning->num_channels < 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_combine_backward(grad_out, y, hidden, L, topk_w, grad_y, grad_w,
+                                                  static_cast<cudaStream_t>(stream), tuning ? tuning->num_channels : 0));
+}
+
 moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* flags_out) {
     if (!L || !L->status) return MOE_ERR_INVALID_ARG;
     uint32_t flags = 0;

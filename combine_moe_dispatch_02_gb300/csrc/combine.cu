@@ -26,8 +26,8 @@ constexpr int kCombineThreads = 256;
 
 struct CombineArgs {
     const uint4* y;              // [n_rows, H/8] of 8 x bf16
-    const int32_t* expert_slot;  // [T, K]
-    const float* w;              // [T, K]
+    const int32_t* expert_slot;  // [T, K]: row of each (t, k), -1 = none
+    const float* w;              // [T, K], or NULL for unit weights
     uint4* out;                  // [T, H/8]
     int32_t T, K, H8;
     int64_t n_rows;
@@ -75,7 +75,7 @@ combine_kernel(CombineArgs a) {
 #pragma unroll
             for (int k = 0; k < KT; ++k) {
                 const int32_t slot = __ldg(a.expert_slot + t * KT + k);
-                ws[k] = __ldg(a.w + t * KT + k);
+                ws[k] = a.w ? __ldg(a.w + t * KT + k) : 1.0f;
                 ok[k] = slot >= 0 && slot < a.n_rows;
                 bad |= slot >= a.n_rows;
                 vals[k] = ok[k] ? ld_stream_v4(a.y + static_cast<int64_t>(slot) * a.H8 + v) : make_uint4(0, 0, 0, 0);
@@ -96,7 +96,7 @@ combine_kernel(CombineArgs a) {
                     vals[q] = make_uint4(0, 0, 0, 0);
                     if (k < a.K) {
                         const int32_t slot = __ldg(a.expert_slot + t * a.K + k);
-                        ws[q] = __ldg(a.w + t * a.K + k);
+                        ws[q] = a.w ? __ldg(a.w + t * a.K + k) : 1.0f;
                         ok[q] = slot >= 0 && slot < a.n_rows;
                         bad |= slot >= a.n_rows;
                         if (ok[q]) vals[q] = ld_stream_v4(a.y + static_cast<int64_t>(slot) * a.H8 + v);
@@ -247,6 +247,29 @@ combine_tma_kernel(CombineArgs a, uint64_t timeout_ns) {
 }
 
 }  // namespace
+
+// Backward of the bf16 dispatch: the same gather with unit weights over the
+// token's receive rows (recv_slot[t, 0..R)), ascending rank order.  With
+// weight 1 the fused multiply-add chain is an fp32 add chain.
+cudaError_t launch_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, const moe_layout* L,
+                                     uint16_t* grad_x, cudaStream_t stream, int32_t num_channels) {
+    if (L->T == 0) return cudaSuccess;
+    CombineArgs a;
+    a.y = reinterpret_cast<const uint4*>(grad_recv);
+    a.expert_slot = L->recv_slot;
+    a.w = nullptr;
+    a.out = reinterpret_cast<uint4*>(grad_x);
+    a.T = L->T; a.K = L->R; a.H8 = hidden / 8;
+    a.n_rows = L->capacity;
+    a.status = L->status;
+    switch (L->R) {
+        case 1: return launch_k<1>(a, stream, num_channels);
+        case 2: return launch_k<2>(a, stream, num_channels);
+        case 4: return launch_k<4>(a, stream, num_channels);
+        case 8: return launch_k<8>(a, stream, num_channels);
+        default: return launch_k<0>(a, stream, num_channels);
+    }
+}
 
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,

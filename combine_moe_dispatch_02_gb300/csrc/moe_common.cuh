@@ -227,6 +227,11 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
                            uint64_t timeout_ns);
+cudaError_t launch_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, const moe_layout* L,
+                                     uint16_t* grad_x, cudaStream_t stream, int32_t num_channels);
+cudaError_t launch_combine_backward(const uint16_t* grad_out, const uint16_t* y, int32_t hidden, const moe_layout* L,
+                                    const float* topk_w, uint16_t* grad_y, float* grad_w, cudaStream_t stream,
+                                    int32_t num_channels);
 LayoutWs layout_workspace(const moe_layout* L);
 size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles);
 int32_t default_tile_tokens(int32_t T, int32_t K);

@@ -39,7 +39,8 @@ MOE_FORMAT_FP8 = 1
 MOE_FORMAT_MXFP8 = 2
 
 EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
-            "moe_dispatch", "moe_combine", "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
+            "moe_dispatch", "moe_combine", "moe_dispatch_backward", "moe_combine_backward",
+            "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
 
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
 
@@ -96,6 +97,11 @@ def lib() -> ctypes.CDLL:
                                    ctypes.POINTER(moe_tuning)]
         L.moe_combine.restype = ctypes.c_int
         L.moe_combine.argtypes = [P, i32, ctypes.POINTER(moe_layout), P, P, P, ctypes.POINTER(moe_tuning)]
+        L.moe_dispatch_backward.restype = ctypes.c_int
+        L.moe_dispatch_backward.argtypes = [P, i32, ctypes.POINTER(moe_layout), P, P, ctypes.POINTER(moe_tuning)]
+        L.moe_combine_backward.restype = ctypes.c_int
+        L.moe_combine_backward.argtypes = [P, P, i32, ctypes.POINTER(moe_layout), P, P, P, P,
+                                           ctypes.POINTER(moe_tuning)]
         L.moe_layout_read_status.restype = ctypes.c_int
         L.moe_layout_read_status.argtypes = [ctypes.POINTER(moe_layout), P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -220,6 +226,21 @@ def moe_combine(y: torch.Tensor, L: Layout, topk_w: torch.Tensor, out: torch.Ten
     assert topk_w.dtype == torch.float32 and topk_w.is_contiguous()
     _check(lib().moe_combine(_ptr(y), y.shape[-1], ctypes.byref(L.c), _ptr(topk_w), _ptr(out),
                              _stream(stream), _tuning(**tuning)), "moe_combine")
+
+
+def moe_dispatch_backward(grad_recv: torch.Tensor, L: Layout, grad_x: torch.Tensor, stream=None, **tuning) -> None:
+    assert grad_recv.dtype == torch.bfloat16 and grad_recv.is_contiguous() and grad_x.is_contiguous()
+    _check(lib().moe_dispatch_backward(_ptr(grad_recv), grad_recv.shape[-1], ctypes.byref(L.c), _ptr(grad_x),
+                                       _stream(stream), _tuning(**tuning)), "moe_dispatch_backward")
+
+
+def moe_combine_backward(grad_out: torch.Tensor, y: torch.Tensor, L: Layout, topk_w: torch.Tensor,
+                         grad_y: torch.Tensor, grad_w: torch.Tensor, stream=None, **tuning) -> None:
+    assert grad_out.dtype == torch.bfloat16 and y.dtype == torch.bfloat16 and topk_w.dtype == torch.float32
+    assert all(t.is_contiguous() for t in (grad_out, y, topk_w, grad_y, grad_w))
+    _check(lib().moe_combine_backward(_ptr(grad_out), _ptr(y), y.shape[-1], ctypes.byref(L.c), _ptr(topk_w),
+                                      _ptr(grad_y), _ptr(grad_w), _stream(stream), _tuning(**tuning)),
+           "moe_combine_backward")
 
 
 def moe_layout_read_status(L: Layout, stream=None) -> tuple[int, int]:

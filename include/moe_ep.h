@@ -215,6 +215,29 @@ moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, 
 moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L,
                        const float* topk_w, uint16_t* out, void* stream, const moe_tuning* tuning);
 
+/* Backward of the bf16 dispatch (its adjoint): grad_x[t,:] = bf16_rne(sum over
+ * r = 0..R-1 with recv_slot[t,r] >= 0 of grad_recv[recv_slot[t,r], :]),
+ * accumulated in fp32 in ascending r (0 for a token sent nowhere).
+ * grad_recv is bf16 [capacity, hidden] (the gradient of the receive rows);
+ * grad_x is bf16 [T, hidden].  hidden % 8 == 0, 16-byte aligned rows.
+ * Training is the pages' workload (Hybrid-EP news article, "Efficiency
+ * Numbers"); they do not describe the backward pass: this is the adjoint of
+ * the forward definition. */
+moe_status moe_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, const moe_layout* L,
+                                 uint16_t* grad_x, void* stream, const moe_tuning* tuning);
+
+/* Backward of moe_combine, from grad_out bf16 [T, hidden]:
+ *   grad_y[expert_slot[t,k], :] = bf16_rne(fp32(topk_w[t,k] * grad_out[t, :]))
+ *   grad_w[t,k] = sum_h grad_out[t,h] * y[expert_slot[t,k], h]   (fp32; 0 if masked)
+ * y and grad_y are bf16 [T*K, hidden] in expert-major row order (rows no
+ * entry maps to are not written); grad_w is fp32 [T, K].  The dot products are
+ * fp32 fused multiply-adds reduced in a fixed order (deterministic), one CTA
+ * per token; their rounding differs from an exact sum by at most about
+ * hidden * 2^-24 * sum_h |grad_out * y|. */
+moe_status moe_combine_backward(const uint16_t* grad_out, const uint16_t* y, int32_t hidden, const moe_layout* L,
+                                const float* topk_w, uint16_t* grad_y, float* grad_w, void* stream,
+                                const moe_tuning* tuning);
+
 /* Synchronise `stream`, read the device status word, and map it to a status
  * (timeout first -- a timed-out scan also makes later kernels see slots out
  * of range -- then expert ids, then capacity).  `flags_out` (may be NULL)

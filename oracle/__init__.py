@@ -85,6 +85,10 @@ def load(path: str) -> ctypes.CDLL:
     L.moe_ref_dispatch_mxfp8.argtypes = [P, i32, i32, i32, P, i64, P, P]
     L.moe_ref_combine.restype = ctypes.c_int
     L.moe_ref_combine.argtypes = [P, i64, i32, i32, i32, P, P, P]
+    L.moe_ref_dispatch_backward.restype = ctypes.c_int
+    L.moe_ref_dispatch_backward.argtypes = [P, i64, i32, i32, i32, P, P]
+    L.moe_ref_combine_backward.restype = ctypes.c_int
+    L.moe_ref_combine_backward.argtypes = [P, P, i64, i32, i32, i32, P, P, P, P]
     return L
 
 
@@ -213,3 +217,33 @@ def combine(y_bits: np.ndarray, expert_slot: np.ndarray, topk_w: np.ndarray):
     out = np.zeros((T, H), np.uint16)
     st = lib().moe_ref_combine(_ptr(y_bits), n_rows, T, K, H, _ptr(expert_slot), _ptr(topk_w), _ptr(out))
     return out, st
+
+
+# ---------------------------------------------------------------- backward
+
+def dispatch_backward(grad_recv_bits: np.ndarray, recv_slot: np.ndarray):
+    """grad_recv uint16 [n_rows,H] bf16.  Returns (grad_x uint16 [T,H], status)."""
+    g = np.ascontiguousarray(grad_recv_bits, dtype=np.uint16)
+    recv_slot = np.ascontiguousarray(recv_slot, dtype=np.int32)
+    n_rows, H = g.shape
+    T, R = recv_slot.shape
+    out = np.zeros((T, H), np.uint16)
+    st = lib().moe_ref_dispatch_backward(_ptr(g), n_rows, T, R, H, _ptr(recv_slot), _ptr(out))
+    return out, st
+
+
+def combine_backward(grad_out_bits: np.ndarray, y_bits: np.ndarray, expert_slot: np.ndarray, topk_w: np.ndarray,
+                     grad_y: np.ndarray | None = None):
+    """Returns (grad_y uint16 [n_rows,H], grad_w float64 [T,K], status); rows of
+    grad_y no entry maps to keep their initial contents (zeros if None)."""
+    go = np.ascontiguousarray(grad_out_bits, dtype=np.uint16)
+    y = np.ascontiguousarray(y_bits, dtype=np.uint16)
+    es = np.ascontiguousarray(expert_slot, dtype=np.int32)
+    w = np.ascontiguousarray(topk_w, dtype=np.float32)
+    n_rows, H = y.shape
+    T, K = es.shape
+    if grad_y is None:
+        grad_y = np.zeros((n_rows, H), np.uint16)
+    gw = np.zeros((T, K), np.float64)
+    st = lib().moe_ref_combine_backward(_ptr(go), _ptr(y), n_rows, T, K, H, _ptr(es), _ptr(w), _ptr(grad_y), _ptr(gw))
+    return grad_y, gw, st

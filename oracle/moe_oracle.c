@@ -308,3 +308,57 @@ int moe_ref_combine(const uint16_t* y, int64_t n_rows, int32_t T, int32_t K,
     free(acc);
     return err;
 }
+
+/* -------------------------------------------------------------- backward */
+
+/* Dispatch copies x[t] to one receive row per destination rank, so its
+ * adjoint sums the gradients of those rows back into token t. */
+int moe_ref_dispatch_backward(const uint16_t* grad_recv, int64_t n_rows, int32_t T, int32_t R,
+                              int32_t H, const int32_t* recv_slot, uint16_t* grad_x)
+{
+    if (!grad_recv || !recv_slot || !grad_x || T < 0 || R <= 0 || H <= 0) return MOE_REF_ERR_ARG;
+    int err = 0;
+    float* acc = (float*)malloc((size_t)H * sizeof(float));
+    if (!acc) return MOE_REF_ERR_ARG;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int32_t h = 0; h < H; ++h) acc[h] = 0.0f;
+        for (int32_t r = 0; r < R; ++r) {
+            int64_t row = recv_slot[t * R + r];
+            if (row < 0) continue;
+            if (row >= n_rows) { err |= MOE_REF_ERR_CAPACITY; continue; }
+            for (int32_t h = 0; h < H; ++h) acc[h] = acc[h] + moe_ref_bf16_decode(grad_recv[row * H + h]);
+        }
+        for (int32_t h = 0; h < H; ++h) grad_x[t * H + h] = moe_ref_bf16_encode(acc[h]);
+    }
+    free(acc);
+    return err;
+}
+
+/* Combine computes out[t] = sum_k w[t,k] * y[slot(t,k)]; its gradients are
+ * w[t,k] * grad_out[t] for the expert rows and <grad_out[t], y[slot(t,k)]>
+ * for the router weights. */
+int moe_ref_combine_backward(const uint16_t* grad_out, const uint16_t* y, int64_t n_rows, int32_t T,
+                             int32_t K, int32_t H, const int32_t* expert_slot, const float* topk_w,
+                             uint16_t* grad_y, double* grad_w)
+{
+    if (!grad_out || !y || !expert_slot || !topk_w || !grad_y || !grad_w || T < 0 || K <= 0 || H <= 0)
+        return MOE_REF_ERR_ARG;
+    int err = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t k = 0; k < K; ++k) {
+            int64_t row = expert_slot[t * K + k];
+            grad_w[t * K + k] = 0.0;
+            if (row < 0) continue;
+            if (row >= n_rows) { err |= MOE_REF_ERR_CAPACITY; continue; }
+            float w = topk_w[t * K + k];
+            double dot = 0.0;
+            for (int32_t h = 0; h < H; ++h) {
+                float g = moe_ref_bf16_decode(grad_out[t * H + h]);
+                float prod = w * g;                                  /* fp32, round to nearest */
+                grad_y[row * H + h] = moe_ref_bf16_encode(prod);
+                dot += (double)g * (double)moe_ref_bf16_decode(y[row * H + h]);
+            }
+            grad_w[t * K + k] = dot;
+        }
+    return err;
+}

@@ -105,6 +105,20 @@ int moe_ref_combine(const uint16_t* y, int64_t n_rows, int32_t T, int32_t K,
                     int32_t H, const int32_t* expert_slot, const float* topk_w,
                     uint16_t* out);
 
+/* Backward of the bf16 dispatch (its adjoint): grad_x[t,:] = bf16_rne(fp32
+ * sum over r ascending of grad_recv[recv_slot[t,r], :]), skipping slots < 0;
+ * 0 for a token sent nowhere.  grad_recv [n_rows,H], grad_x [T,H] bf16 bits. */
+int moe_ref_dispatch_backward(const uint16_t* grad_recv, int64_t n_rows, int32_t T, int32_t R,
+                              int32_t H, const int32_t* recv_slot, uint16_t* grad_x);
+
+/* Backward of combine: grad_y[expert_slot[t,k], :] = bf16_rne(fp32(topk_w[t,k]
+ * * grad_out[t,:])) and grad_w[t,k] = sum_h grad_out[t,h] * y[expert_slot[t,k],h]
+ * accumulated in double (masked entries: 0).  grad_out [T,H], y and grad_y
+ * [n_rows,H] bf16 bits; grad_w [T,K] double. */
+int moe_ref_combine_backward(const uint16_t* grad_out, const uint16_t* y, int64_t n_rows, int32_t T,
+                             int32_t K, int32_t H, const int32_t* expert_slot, const float* topk_w,
+                             uint16_t* grad_y, double* grad_w);
+
 #ifdef __cplusplus
 }
 #endif
