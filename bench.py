@@ -297,6 +297,29 @@ def run_ours(args, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st} after the secondary legs")
 
+    # low-latency (decode) path: 128 tokens of the same shape, fixed capacity 128 per expert
+    T_ll = 128
+    x_ll, idx_ll, w_ll = x[:T_ll].contiguous(), idx[:T_ll].contiguous(), w[:T_ll].contiguous()
+    recv_ll = torch.empty(E * T_ll, H, dtype=torch.bfloat16, device=dev)
+    tpe_ll = torch.empty(E, dtype=torch.int32, device=dev)
+    slot_ll = torch.empty(T_ll, K, dtype=torch.int32, device=dev)
+    st_ll = torch.zeros(1, dtype=torch.int32, device=dev)
+    out_ll = torch.empty(T_ll, H, dtype=torch.bfloat16, device=dev)
+    evl = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(args.steps // 4, 3))]
+    for e in evl:
+        flush()
+        e[0].record(stream)
+        ep.moe_ll_dispatch(x_ll, idx_ll, E, T_ll, recv_ll, tpe_ll, slot_ll, st_ll, stream)
+        e[1].record(stream)
+        ep.moe_ll_combine(recv_ll, slot_ll, w_ll, E, T_ll, out_ll, st_ll, stream)
+        e[2].record(stream)
+    torch.cuda.synchronize(dev)
+    if int(st_ll.item()) != 0:
+        raise RuntimeError("low-latency path reported a device error")
+    lld = [e[0].elapsed_time(e[1]) for e in evl]
+    llc = [e[1].elapsed_time(e[2]) for e in evl]
+    ll_bytes = 2 * T_ll * H + 2 * H * T_ll * K + 4 * T_ll * K    # rows read, one row per entry written
+
     e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if rank == 0 else None
 
     peak, peak_kind = measured_peaks()
@@ -339,6 +362,10 @@ def run_ours(args, rank, world, local_rank):
             "dispatch_backward": {"us": round(statistics.mean(dbwd) * 1e3, 2), "bytes": ab["dispatch_backward"],
                                   "GB/s": round(gbps(ab["dispatch_backward"], statistics.mean(dbwd)), 1),
                                   "frac": round(gbps(ab["dispatch_backward"], statistics.mean(dbwd)) / peak, 4)},
+            "ll_dispatch_T128": {"us": round(statistics.mean(lld) * 1e3, 2), "bytes": ll_bytes,
+                                 "GB/s": round(gbps(ll_bytes, statistics.mean(lld)), 1)},
+            "ll_combine_T128": {"us": round(statistics.mean(llc) * 1e3, 2), "bytes": ll_bytes,
+                                "GB/s": round(gbps(ll_bytes, statistics.mean(llc)), 1)},
             "combine_backward": {"us": round(statistics.mean(cbwd) * 1e3, 2), "bytes": ab["combine_backward"],
                                  "GB/s": round(gbps(ab["combine_backward"], statistics.mean(cbwd)), 1),
                                  "frac": round(gbps(ab["combine_backward"], statistics.mean(cbwd)) / peak, 4)},

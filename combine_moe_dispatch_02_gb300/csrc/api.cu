@@ -178,6 +178,35 @@ moe_status moe_combine_backward(const uint16_t* grad_out, const uint16_t* y, int
                                                   static_cast<cudaStream_t>(stream), tuning ? tuning->num_channels : 0));
 }
 
+moe_status moe_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32_t T, int32_t K, int32_t E, int32_t hidden,
+                           int32_t cap_per_expert, uint16_t* recv, int32_t* tokens_per_expert, int32_t* ll_slot,
+                           uint32_t* status, void* stream, const moe_tuning* tuning) {
+    if (T < 0 || K < 1 || E < 1 || hidden <= 0 || hidden % 8 != 0 || cap_per_expert < 0) return MOE_ERR_INVALID_ARG;
+    if (K > MOE_MAX_TOPK || E > MOE_MAX_EXPERTS) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(T) * K > moe::ll_max_entries()) return MOE_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * cap_per_expert > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if (!tokens_per_expert || !status) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!x || !topk_idx || !ll_slot || (cap_per_expert > 0 && !recv))) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(recv)) return MOE_ERR_INVALID_ARG;
+    if (tuning && tuning->num_channels < 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_ll_dispatch(x, topk_idx, T, K, E, hidden, cap_per_expert, recv, tokens_per_expert,
+                                             ll_slot, status, static_cast<cudaStream_t>(stream),
+                                             tuning ? tuning->num_channels : 0));
+}
+
+moe_status moe_ll_combine(const uint16_t* y, const int32_t* ll_slot, const float* topk_w, int32_t T, int32_t K,
+                          int32_t E, int32_t hidden, int32_t cap_per_expert, uint16_t* out, uint32_t* status,
+                          void* stream, const moe_tuning* tuning) {
+    if (T < 0 || K < 1 || E < 1 || hidden <= 0 || hidden % 8 != 0 || cap_per_expert < 0) return MOE_ERR_INVALID_ARG;
+    if (!status) return MOE_ERR_INVALID_ARG;
+    if (T > 0 && (!y || !ll_slot || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
+    if (!aligned16(y) || !aligned16(out) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) != 0) return MOE_ERR_INVALID_ARG;
+    if (tuning && tuning->num_channels < 0) return MOE_ERR_INVALID_ARG;
+    return from_cuda(moe::launch_ll_combine(y, ll_slot, topk_w, T, K, static_cast<int64_t>(E) * cap_per_expert, hidden,
+                                            out, status, static_cast<cudaStream_t>(stream),
+                                            tuning ? tuning->num_channels : 0));
+}
+
 moe_status moe_layout_read_status(const moe_layout* L, void* stream, uint32_t* flags_out) {
     if (!L || !L->status) return MOE_ERR_INVALID_ARG;
     uint32_t flags = 0;

@@ -271,6 +271,30 @@ cudaError_t launch_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, 
     }
 }
 
+// Combine over the low-latency layout: the same weighted gather, with the
+// slot map ll_slot into y [E * cap, H].
+cudaError_t launch_ll_combine(const uint16_t* y, const int32_t* ll_slot, const float* topk_w, int32_t T, int32_t K,
+                              int64_t n_rows, int32_t hidden, uint16_t* out, uint32_t* status, cudaStream_t stream,
+                              int32_t num_channels) {
+    if (T == 0) return cudaSuccess;
+    CombineArgs a;
+    a.y = reinterpret_cast<const uint4*>(y);
+    a.expert_slot = ll_slot;
+    a.w = topk_w;
+    a.out = reinterpret_cast<uint4*>(out);
+    a.T = T; a.K = K; a.H8 = hidden / 8;
+    a.n_rows = n_rows;
+    a.status = status;
+    switch (K) {
+        case 1: return launch_k<1>(a, stream, num_channels);
+        case 2: return launch_k<2>(a, stream, num_channels);
+        case 4: return launch_k<4>(a, stream, num_channels);
+        case 6: return launch_k<6>(a, stream, num_channels);
+        case 8: return launch_k<8>(a, stream, num_channels);
+        default: return launch_k<0>(a, stream, num_channels);
+    }
+}
+
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
                            uint64_t timeout_ns) {

@@ -232,6 +232,13 @@ cudaError_t launch_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, 
 cudaError_t launch_combine_backward(const uint16_t* grad_out, const uint16_t* y, int32_t hidden, const moe_layout* L,
                                     const float* topk_w, uint16_t* grad_y, float* grad_w, cudaStream_t stream,
                                     int32_t num_channels);
+int32_t ll_max_entries();
+cudaError_t launch_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32_t T, int32_t K, int32_t E,
+                               int32_t hidden, int32_t cap, uint16_t* recv, int32_t* tokens_per_expert,
+                               int32_t* ll_slot, uint32_t* status, cudaStream_t stream, int32_t num_channels);
+cudaError_t launch_ll_combine(const uint16_t* y, const int32_t* ll_slot, const float* topk_w, int32_t T, int32_t K,
+                              int64_t n_rows, int32_t hidden, uint16_t* out, uint32_t* status, cudaStream_t stream,
+                              int32_t num_channels);
 LayoutWs layout_workspace(const moe_layout* L);
 size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles);
 int32_t default_tile_tokens(int32_t T, int32_t K);

@@ -40,6 +40,7 @@ MOE_FORMAT_MXFP8 = 2
 
 EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
             "moe_dispatch", "moe_combine", "moe_dispatch_backward", "moe_combine_backward",
+            "moe_ll_dispatch", "moe_ll_combine",
             "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
 
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
@@ -102,6 +103,10 @@ def lib() -> ctypes.CDLL:
         L.moe_combine_backward.restype = ctypes.c_int
         L.moe_combine_backward.argtypes = [P, P, i32, ctypes.POINTER(moe_layout), P, P, P, P,
                                            ctypes.POINTER(moe_tuning)]
+        L.moe_ll_dispatch.restype = ctypes.c_int
+        L.moe_ll_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P, P, P, ctypes.POINTER(moe_tuning)]
+        L.moe_ll_combine.restype = ctypes.c_int
+        L.moe_ll_combine.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, P, P, ctypes.POINTER(moe_tuning)]
         L.moe_layout_read_status.restype = ctypes.c_int
         L.moe_layout_read_status.argtypes = [ctypes.POINTER(moe_layout), P, ctypes.POINTER(ctypes.c_uint32)]
         L.moe_status_string.restype = ctypes.c_char_p
@@ -241,6 +246,27 @@ def moe_combine_backward(grad_out: torch.Tensor, y: torch.Tensor, L: Layout, top
     _check(lib().moe_combine_backward(_ptr(grad_out), _ptr(y), y.shape[-1], ctypes.byref(L.c), _ptr(topk_w),
                                       _ptr(grad_y), _ptr(grad_w), _stream(stream), _tuning(**tuning)),
            "moe_combine_backward")
+
+
+def moe_ll_dispatch(x: torch.Tensor, topk_idx: torch.Tensor, E: int, cap: int, recv: torch.Tensor,
+                    tokens_per_expert: torch.Tensor, ll_slot: torch.Tensor, status: torch.Tensor, stream=None,
+                    **tuning) -> None:
+    T, H = x.shape
+    K = topk_idx.shape[1]
+    assert x.dtype == torch.bfloat16 and topk_idx.dtype == torch.int32
+    assert all(t.is_contiguous() for t in (x, topk_idx, recv, tokens_per_expert, ll_slot, status))
+    _check(lib().moe_ll_dispatch(_ptr(x), _ptr(topk_idx), T, K, E, H, cap, _ptr(recv), _ptr(tokens_per_expert),
+                                 _ptr(ll_slot), _ptr(status), _stream(stream), _tuning(**tuning)), "moe_ll_dispatch")
+
+
+def moe_ll_combine(y: torch.Tensor, ll_slot: torch.Tensor, topk_w: torch.Tensor, E: int, cap: int,
+                   out: torch.Tensor, status: torch.Tensor, stream=None, **tuning) -> None:
+    T, K = ll_slot.shape
+    H = y.shape[-1]
+    assert y.dtype == torch.bfloat16 and topk_w.dtype == torch.float32
+    assert all(t.is_contiguous() for t in (y, ll_slot, topk_w, out, status))
+    _check(lib().moe_ll_combine(_ptr(y), _ptr(ll_slot), _ptr(topk_w), T, K, E, H, cap, _ptr(out), _ptr(status),
+                                _stream(stream), _tuning(**tuning)), "moe_ll_combine")
 
 
 def moe_layout_read_status(L: Layout, stream=None) -> tuple[int, int]:

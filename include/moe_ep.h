@@ -215,6 +215,31 @@ moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, 
 moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L,
                        const float* topk_w, uint16_t* out, void* stream, const moe_tuning* tuning);
 
+/* Low-latency (decode) dispatch into a fixed-capacity per-expert buffer.
+ * DeepEP pairs its high-throughput kernels with low-latency ones for decode
+ * ("Inside the Nebius + PyTorch DeepSeek V3 recipe", section "DeepEP"); their
+ * receive buffer has a static shape so the experts run on fixed-size inputs.
+ * Here every valid entry (t,k) of expert e = topk_idx[t,k] is written to row
+ * e * cap_per_expert + j of recv bf16 [E, cap_per_expert, hidden], j = the
+ * entry's position among e's entries in (t,k) order (each token once per
+ * expert, not per rank).  Entries with j >= cap_per_expert are dropped
+ * (ll_slot -1, MOE_DEVERR_CAPACITY).  Outputs: tokens_per_expert[E] = rows
+ * written, ll_slot int32 [T,K] = row or -1, and the device status word
+ * *status (MOE_DEVERR_* bits, overwritten by this call).  One launch, no
+ * workspace: T * K <= 4096 (MOE_ERR_UNSUPPORTED beyond).  Rows of recv that
+ * receive nothing are not written. */
+moe_status moe_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32_t T, int32_t K, int32_t E, int32_t hidden,
+                           int32_t cap_per_expert, uint16_t* recv, int32_t* tokens_per_expert, int32_t* ll_slot,
+                           uint32_t* status, void* stream, const moe_tuning* tuning);
+
+/* Combine over the low-latency layout: out[t,:] = bf16_rne(fp32 fused
+ * multiply-add chain over k ascending of topk_w[t,k] * y[ll_slot[t,k], :]),
+ * skipping ll_slot < 0; y is bf16 [E, cap_per_expert, hidden].  Slots past the
+ * buffer set MOE_DEVERR_CAPACITY in *status (OR-ed in) and are skipped. */
+moe_status moe_ll_combine(const uint16_t* y, const int32_t* ll_slot, const float* topk_w, int32_t T, int32_t K,
+                          int32_t E, int32_t hidden, int32_t cap_per_expert, uint16_t* out, uint32_t* status,
+                          void* stream, const moe_tuning* tuning);
+
 /* Backward of the bf16 dispatch (its adjoint): grad_x[t,:] = bf16_rne(sum over
  * r = 0..R-1 with recv_slot[t,r] >= 0 of grad_recv[recv_slot[t,r], :]),
  * accumulated in fp32 in ascending r (0 for a token sent nowhere).

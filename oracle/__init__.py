@@ -85,6 +85,8 @@ def load(path: str) -> ctypes.CDLL:
     L.moe_ref_dispatch_mxfp8.argtypes = [P, i32, i32, i32, P, i64, P, P]
     L.moe_ref_combine.restype = ctypes.c_int
     L.moe_ref_combine.argtypes = [P, i64, i32, i32, i32, P, P, P]
+    L.moe_ref_ll_dispatch.restype = ctypes.c_int
+    L.moe_ref_ll_dispatch.argtypes = [P, P, i32, i32, i32, i32, i32, P, P, P]
     L.moe_ref_dispatch_backward.restype = ctypes.c_int
     L.moe_ref_dispatch_backward.argtypes = [P, i64, i32, i32, i32, P, P]
     L.moe_ref_combine_backward.restype = ctypes.c_int
@@ -247,3 +249,19 @@ def combine_backward(grad_out_bits: np.ndarray, y_bits: np.ndarray, expert_slot:
     gw = np.zeros((T, K), np.float64)
     st = lib().moe_ref_combine_backward(_ptr(go), _ptr(y), n_rows, T, K, H, _ptr(es), _ptr(w), _ptr(grad_y), _ptr(gw))
     return grad_y, gw, st
+
+
+# ------------------------------------------------------------- low latency
+
+def ll_dispatch(x_bits: np.ndarray, topk_idx: np.ndarray, E: int, cap: int, recv: np.ndarray | None = None):
+    """Returns (recv uint16 [E*cap,H], tokens_per_expert int32 [E], ll_slot int32 [T,K], status)."""
+    x_bits = np.ascontiguousarray(x_bits, dtype=np.uint16)
+    idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, H = x_bits.shape
+    K = idx.shape[1]
+    if recv is None:
+        recv = np.zeros((E * cap, H), np.uint16)
+    tpe = np.zeros(E, np.int32)
+    slot = np.zeros((T, K), np.int32)
+    st = lib().moe_ref_ll_dispatch(_ptr(x_bits), _ptr(idx), T, K, E, H, cap, _ptr(recv), _ptr(tpe), _ptr(slot))
+    return recv, tpe, slot, st

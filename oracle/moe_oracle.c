@@ -362,3 +362,35 @@ int moe_ref_combine_backward(const uint16_t* grad_out, const uint16_t* y, int64_
         }
     return err;
 }
+
+/* ------------------------------------------------------------ low latency */
+
+int moe_ref_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32_t T, int32_t K, int32_t E,
+                        int32_t H, int32_t cap, uint16_t* recv, int32_t* tokens_per_expert,
+                        int32_t* ll_slot)
+{
+    if (!x || !topk_idx || !recv || !tokens_per_expert || !ll_slot || T < 0 || K <= 0 || E <= 0 || H <= 0 || cap < 0)
+        return MOE_REF_ERR_ARG;
+    int err = 0;
+    for (int32_t e = 0; e < E; ++e) tokens_per_expert[e] = 0;
+    for (int64_t t = 0; t < T; ++t)
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t e = topk_idx[t * K + k];
+            int32_t slot = -1;
+            if (e < -1 || e >= E) {
+                err |= MOE_REF_ERR_EXPERT_ID;
+            } else if (e >= 0) {
+                /* tokens_per_expert[e] counts the earlier entries of e so far */
+                int32_t j = tokens_per_expert[e];
+                if (j < cap) {
+                    slot = e * cap + j;
+                    tokens_per_expert[e] = j + 1;
+                    memcpy(recv + (int64_t)slot * H, x + t * H, (size_t)H * sizeof(uint16_t));
+                } else {
+                    err |= MOE_REF_ERR_CAPACITY;
+                }
+            }
+            ll_slot[t * K + k] = slot;
+        }
+    return err;
+}

@@ -105,6 +105,18 @@ int moe_ref_combine(const uint16_t* y, int64_t n_rows, int32_t T, int32_t K,
                     int32_t H, const int32_t* expert_slot, const float* topk_w,
                     uint16_t* out);
 
+/* Low-latency dispatch (DeepEP's low-latency family, "Inside the Nebius +
+ * PyTorch DeepSeek V3 recipe", section "DeepEP"): every valid entry (t,k) is
+ * written to a fixed-capacity per-expert buffer recv [E, cap, H] at row
+ * e * cap + j, j = #{(t',k') < (t,k) : idx[t',k'] == e}; entries with
+ * j >= cap are dropped (ll_slot -1, MOE_REF_ERR_CAPACITY).  Outputs:
+ * tokens_per_expert[E] (rows written), ll_slot[T,K] (row or -1).  Rows of
+ * recv that receive nothing keep their contents.  The combine for this layout
+ * is moe_ref_combine with ll_slot as the slot map. */
+int moe_ref_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32_t T, int32_t K, int32_t E,
+                        int32_t H, int32_t cap, uint16_t* recv, int32_t* tokens_per_expert,
+                        int32_t* ll_slot);
+
 /* Backward of the bf16 dispatch (its adjoint): grad_x[t,:] = bf16_rne(fp32
  * sum over r ascending of grad_recv[recv_slot[t,r], :]), skipping slots < 0;
  * 0 for a token sent nowhere.  grad_recv [n_rows,H], grad_x [T,H] bf16 bits. */
