@@ -17,9 +17,14 @@
 //     stage (mbarrier transaction counting), `stages` items ahead;
 //   * bf16: one TMA bulk store per destination row streams the stage back out
 //     (lanes of the warp issue the stores of different ranks in parallel);
-//   * FP8: the CTA's warps compute block amax, scale and E4M3 codes into an
-//     output stage, which TMA bulk stores send to every destination row; the
-//     scales go out with plain stores.
+//   * FP8 (TMA variant): the CTA's warps compute block amax, scale and E4M3
+//     codes into an output stage, which TMA bulk stores send to every
+//     destination row; the scales go out with plain stores.
+// FP8 and MXFP8 default to the 16-byte vector kernel further down (no staging:
+// each warp quantises 512-column segments in registers and stores the codes
+// straight to every destination row), which measured fastest for them on
+// GB300; bf16 defaults to the TMA kernel.  A warp-specialised TMA variant
+// (one copy warp, eight quantiser warps) is kept as variant 3.
 // x is read from HBM once; the receive rows are written once each.
 #include <climits>
 
@@ -282,6 +287,195 @@ dispatch_fp8_kernel(DispatchArgs a) {
     if (timed_out && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
 }
 
+// Warp-specialised FP8 path --------------------------------------------------
+//
+// Roles inside one CTA, linked by mbarriers only (no CTA-wide barrier per
+// item, so a slow warp delays only the store of its own item):
+//   warp 0 (producer): TMA bulk loads of items into an input ring of
+//     kWsInStages stages, and -- once an item is quantised -- one TMA bulk
+//     store of the code row per destination plus the scale words; it prefetches
+//     the next token's recv_slot row into a register while the current one is
+//     being stored;
+//   warps 1..kWsQuant (quantisers): each takes every kWsQuant-th group of four
+//     128-column blocks of an item, reads the bf16 input stage, writes the code
+//     stage and the scale words.
+// Barriers per stage: in_full (TMA bytes), in_empty (one arrive per quantiser
+// warp), out_full (one arrive per quantiser warp), out_empty (producer, after
+// the bulk stores have read the stage).  Every wait is bounded.
+constexpr int kWsQuant = 8;
+constexpr int kWsThreads = 32 * (1 + kWsQuant);
+constexpr int kWsInStages = 4;
+constexpr int kWsOutStages = 3;
+
+template <int FMT>
+__global__ void __launch_bounds__(kWsThreads)
+dispatch_fp8_ws_kernel(DispatchArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    pdl_wait();
+    const ItemRange rg = channel_items(a);
+    if (rg.n <= 0) return;
+    uint64_t* in_full = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* in_empty = in_full + kWsInStages;
+    uint64_t* out_full = in_empty + kWsInStages;
+    uint64_t* out_empty = out_full + kWsOutStages;
+    const int nbc = a.chunk_elems / 128;                      // 128-column groups per chunk
+    uint32_t* s_scale = reinterpret_cast<uint32_t*>(smem + 256);            // [kWsOutStages][nbc]
+    uint8_t* stage_in = smem + 256 + align_up(sizeof(uint32_t) * kWsOutStages * nbc, 128);
+    const uint32_t in_bytes = static_cast<uint32_t>(a.chunk_elems) * 2u;
+    uint8_t* stage_out = stage_in + static_cast<size_t>(kWsInStages) * in_bytes;
+    const uint32_t out_bytes = static_cast<uint32_t>(a.chunk_elems);
+    const int64_t x_row_bytes = static_cast<int64_t>(a.H) * 2;
+    const int nb_row = a.H / 128;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    if (tid == 0) {
+        for (int s = 0; s < kWsInStages; ++s) { mbar_init(&in_full[s], 1); mbar_init(&in_empty[s], kWsQuant); }
+        for (int s = 0; s < kWsOutStages; ++s) { mbar_init(&out_full[s], kWsQuant); mbar_init(&out_empty[s], 1); }
+        fence_mbar_init();
+    }
+    __syncthreads();
+
+    auto item_of = [&](int k, int64_t* t, int* c, int* elems) {
+        const int64_t i = rg.i0 + k;
+        *t = i / a.nchunk;
+        *c = static_cast<int>(i - *t * a.nchunk);
+        *elems = min(a.chunk_elems, a.H - *c * a.chunk_elems);
+    };
+    bool timed_out = false, bad = false;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ producer
+        auto issue_load = [&](int k) {           // lane 0 only
+            int64_t t; int c, elems;
+            item_of(k, &t, &c, &elems);
+            const int s = k % kWsInStages;
+            mbar_arrive_expect_tx(&in_full[s], static_cast<uint32_t>(elems) * 2u);
+            bulk_g2s(stage_in + static_cast<size_t>(s) * in_bytes,
+                     a.x + t * x_row_bytes + static_cast<int64_t>(c) * a.chunk_elems * 2,
+                     static_cast<uint32_t>(elems) * 2u, &in_full[s]);
+        };
+        if (lane == 0)
+            for (int k = 0; k < kWsInStages - 1 && k < rg.n; ++k) issue_load(k);
+        int issued = min(kWsInStages - 1, rg.n);               // warp-uniform
+        int64_t t_cur; int c_cur, e_cur;
+        item_of(0, &t_cur, &c_cur, &e_cur);
+        int32_t slot_next = (a.R <= 32 && lane < a.R) ? __ldg(a.recv_slot + t_cur * a.R + lane) : -1;
+        int64_t slot_tok = t_cur;
+        for (int k = 0; k < rg.n; ++k) {
+            int64_t t; int c, elems;
+            item_of(k, &t, &c, &elems);
+            // keep the input ring kWsInStages - 1 items ahead
+            const int kl = k + kWsInStages - 1;
+            if (kl < rg.n) {
+                bool ok = true;
+                if (kl >= kWsInStages)
+                    ok = mbar_wait_bounded(&in_empty[kl % kWsInStages],
+                                           static_cast<uint32_t>(kl / kWsInStages - 1) & 1u, a.timeout_ns);
+                if (__any_sync(0xffffffffu, !ok)) { timed_out = true; break; }
+                if (lane == 0) { fence_proxy_async_smem(); issue_load(kl); }
+                ++issued;
+            }
+            // slots of this item's token (prefetched when the token started)
+            int32_t my_slot = slot_next;
+            if (t != slot_tok) {
+                my_slot = (a.R <= 32 && lane < a.R) ? __ldg(a.recv_slot + t * a.R + lane) : -1;
+            }
+            // prefetch the slots of the next item's token
+            if (k + 1 < rg.n) {
+                int64_t tn; int cn, en;
+                item_of(k + 1, &tn, &cn, &en);
+                if (tn != t) slot_next = (a.R <= 32 && lane < a.R) ? __ldg(a.recv_slot + tn * a.R + lane) : -1;
+                else slot_next = my_slot;
+                slot_tok = tn;
+            }
+            const int o = k % kWsOutStages;
+            const bool got = mbar_wait_bounded(&out_full[o], static_cast<uint32_t>(k / kWsOutStages) & 1u, a.timeout_ns);
+            if (__any_sync(0xffffffffu, !got)) { timed_out = true; break; }
+            const int nb = elems / 128;
+            const uint8_t* outp = stage_out + static_cast<size_t>(o) * out_bytes;
+            for (int rbase = 0; rbase < a.R; rbase += 32) {
+                const int32_t sl = (a.R <= 32) ? my_slot
+                                               : (rbase + lane < a.R ? __ldg(a.recv_slot + t * a.R + rbase + lane) : -1);
+                if (sl >= a.capacity) bad = true;
+                if (sl >= 0 && sl < a.capacity)
+                    bulk_s2g(a.recv + static_cast<int64_t>(sl) * a.H + static_cast<int64_t>(c) * a.chunk_elems, outp,
+                             static_cast<uint32_t>(elems));
+                // scale words of this chunk to every destination
+                const int nr = min(32, a.R - rbase);
+                for (int r = 0; r < nr; ++r) {
+                    const int32_t sr = __shfl_sync(0xffffffffu, sl, r);
+                    if (sr < 0 || sr >= a.capacity) continue;
+                    for (int b = lane; b < nb; b += 32)
+                        a.recv_scales[static_cast<int64_t>(sr) * nb_row + c * nbc + b] = s_scale[o * nbc + b];
+                }
+            }
+            bulk_commit();
+            // release the output stage of the previous item once its stores have read it
+            if (k >= 1) {
+                bulk_wait_read<1>();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&out_empty[(k - 1) % kWsOutStages]);
+            }
+        }
+        bulk_wait_all();
+        // After a timeout, loads may still be landing in the input ring: wait
+        // (bounded) for the last load issued into each stage before exiting.
+        for (int s = 0; s < kWsInStages && s < issued; ++s) {
+            const int j = s + (issued - 1 - s) / kWsInStages * kWsInStages;
+            if (!mbar_wait_bounded(&in_full[s], static_cast<uint32_t>(j / kWsInStages) & 1u, a.timeout_ns))
+                timed_out = true;
+        }
+    } else {
+        // ----------------------------------------------------------- quantisers
+        const int q = warp - 1;
+        const int li = lane & 7;
+        for (int k = 0; k < rg.n; ++k) {
+            int64_t t; int c, elems;
+            item_of(k, &t, &c, &elems);
+            const int s = k % kWsInStages, o = k % kWsOutStages;
+            bool ok = mbar_wait_bounded(&in_full[s], static_cast<uint32_t>(k / kWsInStages) & 1u, a.timeout_ns);
+            if (ok && k >= kWsOutStages)
+                ok = mbar_wait_bounded(&out_empty[o], static_cast<uint32_t>(k / kWsOutStages - 1) & 1u, a.timeout_ns);
+            if (__any_sync(0xffffffffu, !ok)) { timed_out = true; break; }
+            const int nb = elems / 128;
+            const uint8_t* in = stage_in + static_cast<size_t>(s) * in_bytes;
+            uint8_t* out = stage_out + static_cast<size_t>(o) * out_bytes;
+            for (int base = q * 4; base < nb; base += 4 * kWsQuant) {
+                const int b = base + (lane >> 3);
+                const bool active = b < nb;
+                uint4 va = make_uint4(0u, 0u, 0u, 0u), vb = va;
+                if (active) {
+                    va = *reinterpret_cast<const uint4*>(in + b * 256 + li * 16);
+                    vb = *reinterpret_cast<const uint4*>(in + b * 256 + 128 + li * 16);
+                }
+                uint2 q0, q1;
+                uint32_t word;
+                if constexpr (FMT == 1) {
+                    const BlockQuant bq = quantize_block_share(va, vb);
+                    q0 = bq.q0; q1 = bq.q1; word = __float_as_uint(bq.scale);
+                } else {
+                    const MxQuant mq = quantize_group_share_mx(va, vb);
+                    q0 = mq.q0; q1 = mq.q1; word = mq.scales;
+                }
+                if (active) {
+                    *reinterpret_cast<uint2*>(out + b * 128 + li * 8) = q0;
+                    *reinterpret_cast<uint2*>(out + b * 128 + 64 + li * 8) = q1;
+                    if (li == 0) s_scale[o * nbc + b] = word;
+                }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&in_empty[s]);
+                mbar_arrive(&out_full[o]);
+            }
+        }
+    }
+    pdl_trigger();
+    if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+    if (__syncthreads_or(timed_out) && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
+}
+
 // 16-byte vector path ------------------------------------------------------
 
 // No shared-memory staging: a warp moves one 512-column segment of one token
@@ -289,8 +483,8 @@ dispatch_fp8_kernel(DispatchArgs a) {
 // instruction of the warp covers whole 32-byte sectors.  bf16: lane l takes
 // columns l*8 and 256 + l*8 of the segment.  FP8: the eight lanes 8g..8g+7
 // hold block g of the segment (lane li: columns li*8 and 64 + li*8 of it) and
-// reduce its amax with shuffles.  Two items are in flight per warp (all their
-// loads are issued before any store).  The destination rows come from
+// reduce its amax with shuffles.  U items (2 or 4) are in flight per warp (all
+// their loads are issued before any store).  The destination rows come from
 // recv_slot: lane r holds the slot of rank r and the warp walks the ranks with
 // shuffles.
 constexpr int kLsuThreads = 256;
@@ -310,7 +504,8 @@ __device__ __forceinline__ int lsu_col(int col0, int lane, int j) {
 }
 
 // FMT 0: bf16 rows; 1: FP8 with fp32 1x128 scales; 2: MXFP8 (E8M0 1x32 scales).
-template <int FMT>
+// U items in flight per warp.
+template <int FMT, int U>
 __global__ void __launch_bounds__(kLsuThreads)
 dispatch_lsu_kernel(DispatchArgs a) {
     pdl_wait();
@@ -321,14 +516,14 @@ dispatch_lsu_kernel(DispatchArgs a) {
     const int64_t n_items = static_cast<int64_t>(a.T) * nseg;
     const int nb_row = a.H / 128;
     bool bad = false;
-    for (int64_t item0 = warp_id; item0 < n_items; item0 += 2 * n_warps) {
-        uint4 v[2][2];
-        int32_t slot_lane[2];
-        int64_t tok[2];
-        int col0[2];
-        bool live[2];
+    for (int64_t item0 = warp_id; item0 < n_items; item0 += U * n_warps) {
+        uint4 v[U][2];
+        int32_t slot_lane[U];
+        int64_t tok[U];
+        int col0[U];
+        bool live[U];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int64_t item = item0 + u * n_warps;
             live[u] = item < n_items;                      // warp-uniform
             const int64_t t = live[u] ? item / nseg : 0;
@@ -343,7 +538,7 @@ dispatch_lsu_kernel(DispatchArgs a) {
             }
         }
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
+        for (int u = 0; u < U; ++u) {
             if (!live[u]) continue;
             const int64_t t = tok[u];
             uint2 q0 = make_uint2(0u, 0u), q1 = q0;
@@ -429,25 +624,57 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     } else {
         smem += static_cast<size_t>(S) * a.chunk_elems * 2;
     }
-    if (variant == 2) {
-        // 16-byte vector path: persistent grid, occupancy-limited
-        const void* fn = format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2>)
-                         : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1>)
-                               : reinterpret_cast<const void*>(dispatch_lsu_kernel<0>);
+    if (variant == 2 || (fp8 && variant == 0)) {
+        // 16-byte vector path (the FP8 / MXFP8 default): persistent grid, occupancy-limited
+        // items in flight per warp: 4 when asked for 4+ stages, else 2
+        const int U = stages >= 4 ? 4 : 2;
+        const void* fn = U == 4 ? (format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2, 4>)
+                                   : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1, 4>)
+                                         : reinterpret_cast<const void*>(dispatch_lsu_kernel<0, 4>))
+                                : (format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2, 2>)
+                                   : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1, 2>)
+                                         : reinterpret_cast<const void*>(dispatch_lsu_kernel<0, 2>));
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLsuThreads, 0);
         if (e != cudaSuccess) return e;
         if (per_sm < 1) per_sm = 1;
         const int64_t nseg = (hidden + kSegElems - 1) / kSegElems;
-        const int64_t warps_needed = (static_cast<int64_t>(L->T) * nseg + 1) / 2;
+        const int64_t warps_needed = (static_cast<int64_t>(L->T) * nseg + U - 1) / U;
         int64_t lsu_grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
         const int64_t need = (warps_needed * 32 + kLsuThreads - 1) / kLsuThreads;
         if (lsu_grid > need) lsu_grid = need;
         if (lsu_grid < 1) lsu_grid = 1;
         const dim3 g(static_cast<unsigned>(lsu_grid)), b(kLsuThreads);
-        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2>, g, b, 0, stream, a);
-        if (fp8) return launch_pdl(dispatch_lsu_kernel<1>, g, b, 0, stream, a);
-        return launch_pdl(dispatch_lsu_kernel<0>, g, b, 0, stream, a);
+        if (U == 4) {
+            if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2, 4>, g, b, 0, stream, a);
+            if (fp8) return launch_pdl(dispatch_lsu_kernel<1, 4>, g, b, 0, stream, a);
+            return launch_pdl(dispatch_lsu_kernel<0, 4>, g, b, 0, stream, a);
+        }
+        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2, 2>, g, b, 0, stream, a);
+        if (fp8) return launch_pdl(dispatch_lsu_kernel<1, 2>, g, b, 0, stream, a);
+        return launch_pdl(dispatch_lsu_kernel<0, 2>, g, b, 0, stream, a);
+    }
+    if (fp8 && variant == 3) {
+        const int nbc = a.chunk_elems / 128;
+        const size_t smem_ws = 256 + align_up(sizeof(uint32_t) * kWsOutStages * nbc, 128) +
+                               static_cast<size_t>(kWsInStages) * a.chunk_elems * 2 +
+                               static_cast<size_t>(kWsOutStages) * a.chunk_elems;
+        const void* fnw = format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_fp8_ws_kernel<2>)
+                                                     : reinterpret_cast<const void*>(dispatch_fp8_ws_kernel<1>);
+        cudaError_t e = cudaFuncSetAttribute(fnw, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_ws));
+        if (e != cudaSuccess) return e;
+        int per_sm = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fnw, kWsThreads, smem_ws);
+        if (e != cudaSuccess) return e;
+        if (per_sm < 1) return cudaErrorInvalidConfiguration;
+        int64_t g = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
+        if (g > n_items) g = n_items;
+        if (g < 1) g = 1;
+        if (format == MOE_FORMAT_MXFP8)
+            return launch_pdl(dispatch_fp8_ws_kernel<2>, dim3(static_cast<unsigned>(g)), dim3(kWsThreads), smem_ws,
+                              stream, a);
+        return launch_pdl(dispatch_fp8_ws_kernel<1>, dim3(static_cast<unsigned>(g)), dim3(kWsThreads), smem_ws,
+                          stream, a);
     }
     const void* fn = format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel<2>)
                      : fp8 ? reinterpret_cast<const void*>(dispatch_fp8_kernel<1>)

@@ -66,9 +66,13 @@ typedef struct moe_tuning {
     int32_t  stages;           /* dispatch pipeline depth per channel, 2..8; 0 = auto             */
     int32_t  chunk_bytes;      /* dispatch: bf16 bytes of a row per pipeline item (a multiple of
                                   256, >= 256); 0 = 16384, i.e. whole rows up to hidden 8192     */
-    int32_t  variant;          /* dispatch / combine kernel: 0 = default, 1 = TMA bulk copies
-                                  staged in shared memory (combine: K <= 8), 2 = 16-byte vector
-                                  loads / stores                                                */
+    int32_t  variant;          /* dispatch / combine kernel: 0 = default (bf16 dispatch: 1;
+                                  FP8 / MXFP8 dispatch: 2; combine: 16-byte vector loads with
+                                  the fma chain in registers), 1 = TMA bulk copies staged in
+                                  shared memory (combine: K <= 8), 2 = 16-byte vector loads /
+                                  stores (combine: as 0), 3 = FP8 / MXFP8 dispatch with
+                                  warp-specialised roles (one TMA warp, eight quantiser warps;
+                                  bf16 dispatch and combine treat 3 as 0)                       */
     uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                   */
     uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                          */
     uint32_t reserved2;

@@ -28,7 +28,7 @@ def test_workload_parity_full_size(name):
     inp = make_inputs(wl)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8)
     assert o["status"] == 0
-    for variant in (0, 1, 2):
+    for variant in (0, 1, 2, 3):
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8, variant=variant)
         assert g["status"] == 0
         assert_parity(g, o, fp8=wl.fp8)
@@ -49,8 +49,9 @@ def test_workload_parity_full_size(name):
     (128, 9216, 16, 4, 4, 0.0, False, True, 9),      # FP8 rows split into chunks
     (2500, 128, 256, 32, 8, 0.0, False, False, 10),  # many tiles, wide ranks
     (4096, 64, 1024, 256, 32, 0.0, False, False, 11),  # the documented maxima of E, R and K
+    (700, 256, 128, 64, 8, 0.1, False, True, 12),   # FP8 with more than 32 destination ranks
 ])
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed, variant):
     idx = random_routing(T, K, E, seed, mask_frac=mask, allow_duplicates=dups)
     w = random_weights(T, K, seed)
@@ -102,7 +103,7 @@ def test_fp8_special_blocks():
     x[5, 256:384] = torch.tensor([1e-38] * 127 + [1.0])
     x = x.to(torch.bfloat16)
     o = oracle_run(x, idx, None, None, E, R, fp8=True)
-    for variant in (1, 2):
+    for variant in (1, 2, 3):
         g = gpu_run(x, idx, None, None, E, R, fp8=True, variant=variant)
         assert_parity(g, o, fp8=True)
 
@@ -148,12 +149,13 @@ def test_tuning_variants_agree():
     inp = make_inputs(wl)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R)
     for ch, st, cb, var in [(1, 2, 0, 1), (4, 3, 2048, 1), (16, 8, 4096, 1), (1000, 0, 0, 1),
-                            (1, 0, 0, 2), (5, 0, 0, 2), (3000, 0, 0, 2)]:
+                            (1, 0, 0, 2), (5, 0, 0, 2), (3000, 0, 0, 2), (0, 4, 0, 2), (7, 4, 0, 2)]:
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, num_channels=ch, stages=st,
                     chunk_bytes=cb, variant=var)
         assert_parity(g, o)
     o8 = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True)
-    for ch, st, cb, var in [(1, 2, 0, 1), (7, 4, 2048, 1), (3, 0, 0, 2), (999, 0, 0, 2)]:
+    for ch, st, cb, var in [(1, 2, 0, 1), (7, 4, 2048, 1), (3, 0, 0, 2), (999, 0, 0, 2),
+                            (1, 0, 0, 3), (7, 0, 2048, 3), (999, 0, 4096, 3), (0, 4, 0, 2), (9, 4, 0, 2)]:
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True, num_channels=ch, stages=st,
                     chunk_bytes=cb, variant=var)
         assert_parity(g, o8, fp8=True)
@@ -175,14 +177,14 @@ def test_mxfp8_parity_full_size(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl, with_y=False)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=2)
-    for variant in (1, 2):
+    for variant in (1, 2, 3):
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=2, variant=variant)
         assert g["status"] == 0
         assert_parity(g, o, fp8=True)
 
 
 @pytest.mark.parametrize("T,H,E,R,K,seed", [(1, 128, 4, 2, 2, 0), (333, 384, 32, 8, 6, 1), (128, 9216, 16, 4, 4, 2)])
-@pytest.mark.parametrize("variant", [1, 2])
+@pytest.mark.parametrize("variant", [1, 2, 3])
 def test_mxfp8_edge_cases(T, H, E, R, K, seed, variant):
     idx = random_routing(T, K, E, seed, mask_frac=0.1)
     g_ = torch.Generator().manual_seed(seed + 5)
