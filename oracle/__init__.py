@@ -77,6 +77,8 @@ def load(path: str) -> ctypes.CDLL:
     L.moe_ref_e4m3_decode.argtypes = [ctypes.c_uint8]
     L.moe_ref_layout.restype = ctypes.c_int
     L.moe_ref_layout.argtypes = [P, P, i32, i32, i32, i32, i64] + [P] * 10
+    L.moe_ref_layout_sources.restype = ctypes.c_int
+    L.moe_ref_layout_sources.argtypes = [P, P, i32, i32, i32, i32, i32] + [P] * 10
     L.moe_ref_dispatch_bf16.restype = ctypes.c_int
     L.moe_ref_dispatch_bf16.argtypes = [P, i32, i32, i32, P, i64, P]
     L.moe_ref_dispatch_fp8.restype = ctypes.c_int
@@ -146,10 +148,13 @@ class Layout:
     expert_src_row: np.ndarray
     expert_weight: np.ndarray
     status: int
+    num_sources: int = 0                           # 0: single-source packed layout
+    recv_source_offset: np.ndarray | None = None   # [R, S+1], multi-source only
 
     @property
     def n_pairs(self) -> int:
-        return int(self.rank_offset[self.R])
+        """Receive rows in use (summed over the destination ranks)."""
+        return int(self.tokens_per_rank.sum())
 
 
 def layout(topk_idx: np.ndarray, topk_w: np.ndarray | None, E: int, R: int,
@@ -168,6 +173,30 @@ def layout(topk_idx: np.ndarray, topk_w: np.ndarray | None, E: int, R: int,
         _ptr(topk_idx), _ptr(w), T, K, E, R, capacity,
         _ptr(L.tokens_per_expert), _ptr(L.expert_offset), _ptr(L.tokens_per_rank),
         _ptr(L.rank_offset), _ptr(L.recv_expert_offset), _ptr(L.recv_slot), _ptr(L.expert_slot),
+        _ptr(L.recv_src_token), _ptr(L.expert_src_row), _ptr(L.expert_weight))
+    return L
+
+
+def layout_sources(topk_idx: np.ndarray, topk_w: np.ndarray | None, S: int, E: int, R: int) -> Layout:
+    """Multi-source receive layout: topk_idx [S*Ts, K] holds the S sources'
+    routing one after the other; capacity is R * T (one region of T rows per
+    destination).  recv_expert_offset is None."""
+    topk_idx = np.ascontiguousarray(topk_idx, dtype=np.int32)
+    T, K = topk_idx.shape
+    assert S >= 1 and T % S == 0, "every source holds the same number of tokens"
+    Ts = T // S
+    capacity = R * T
+    w = None if topk_w is None else np.ascontiguousarray(topk_w, dtype=np.float32)
+    i32 = np.int32
+    L = Layout(T, K, E, R, capacity,
+               np.zeros(E, i32), np.zeros(E + 1, i32), np.zeros(R, i32), np.zeros(R + 1, i32),
+               None, np.zeros((T, R), i32), np.zeros((T, K), i32),
+               np.zeros(capacity, i32), np.zeros(T * K, i32), np.zeros(T * K, np.float32), 0,
+               num_sources=S, recv_source_offset=np.zeros((R, S + 1), i32))
+    L.status = lib().moe_ref_layout_sources(
+        _ptr(topk_idx), _ptr(w), S, Ts, K, E, R,
+        _ptr(L.tokens_per_expert), _ptr(L.expert_offset), _ptr(L.tokens_per_rank),
+        _ptr(L.rank_offset), _ptr(L.recv_source_offset), _ptr(L.recv_slot), _ptr(L.expert_slot),
         _ptr(L.recv_src_token), _ptr(L.expert_src_row), _ptr(L.expert_weight))
     return L
 

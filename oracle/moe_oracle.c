@@ -184,6 +184,92 @@ int moe_ref_layout(const int32_t* topk_idx, const float* topk_w,
     return err;
 }
 
+/* ------------------------------------------------- multi-source layout */
+
+/* Does token g have a valid expert on rank r? */
+static int reaches_rank(const int32_t* topk_idx, int64_t g, int32_t K, int32_t E, int32_t m, int32_t r)
+{
+    for (int32_t k = 0; k < K; ++k) {
+        int32_t e = topk_idx[g * K + k];
+        if (e >= 0 && e < E && e / m == r) return 1;
+    }
+    return 0;
+}
+
+int moe_ref_layout_sources(const int32_t* topk_idx, const float* topk_w,
+                           int32_t S, int32_t Ts, int32_t K, int32_t E, int32_t R,
+                           int32_t* tokens_per_expert, int32_t* expert_offset,
+                           int32_t* tokens_per_rank, int32_t* rank_offset,
+                           int32_t* recv_source_offset, int32_t* recv_slot,
+                           int32_t* expert_slot, int32_t* recv_src_token,
+                           int32_t* expert_src_row, float* expert_weight)
+{
+    if (S <= 0 || Ts < 0 || K <= 0 || E <= 0 || R <= 0 || E % R != 0) return MOE_REF_ERR_ARG;
+    if (!topk_idx || !tokens_per_expert || !expert_offset || !tokens_per_rank || !rank_offset ||
+        !recv_source_offset || !recv_slot || !expert_slot || !recv_src_token || !expert_src_row)
+        return MOE_REF_ERR_ARG;
+    const int32_t m = E / R;
+    const int64_t T = (int64_t)S * Ts;
+    int err = 0;
+    int32_t* seen = (int32_t*)calloc((size_t)E, sizeof(int32_t));
+    if (!seen) return MOE_REF_ERR_ARG;
+
+    /* per-expert counts and offsets, as in the single-source layout */
+    for (int32_t e = 0; e < E; ++e) tokens_per_expert[e] = 0;
+    for (int64_t g = 0; g < T; ++g)
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t e = topk_idx[g * K + k];
+            if (e == -1) continue;
+            if (e < -1 || e >= E) { err |= MOE_REF_ERR_EXPERT_ID; continue; }
+            tokens_per_expert[e] += 1;
+        }
+    expert_offset[0] = 0;
+    for (int32_t e = 0; e < E; ++e) expert_offset[e + 1] = expert_offset[e] + tokens_per_expert[e];
+
+    /* destination regions: each rank walks the tokens in (source, token)
+     * order and takes the ones that reach it, one row each */
+    for (int64_t i = 0; i < (int64_t)R * T; ++i) recv_src_token[i] = -1;
+    for (int32_t r = 0; r < R; ++r) {
+        int32_t used = 0;
+        for (int32_t s = 0; s < S; ++s) {
+            recv_source_offset[(int64_t)r * (S + 1) + s] = used;
+            for (int32_t t = 0; t < Ts; ++t) {
+                int64_t g = (int64_t)s * Ts + t;
+                int32_t slot = -1;
+                if (reaches_rank(topk_idx, g, K, E, m, r)) {
+                    slot = (int32_t)((int64_t)r * T + used);
+                    recv_src_token[slot] = (int32_t)g;
+                    used += 1;
+                }
+                recv_slot[g * R + r] = slot;
+            }
+        }
+        recv_source_offset[(int64_t)r * (S + 1) + S] = used;
+        tokens_per_rank[r] = used;
+        rank_offset[r] = (int32_t)((int64_t)r * T);
+    }
+    rank_offset[R] = (int32_t)((int64_t)R * T);
+
+    /* expert-major rows ordered by (expert, token, k), as in the
+     * single-source layout */
+    for (int64_t i = 0; i < T * K; ++i) {
+        expert_src_row[i] = -1;
+        if (topk_w && expert_weight) expert_weight[i] = 0.0f;
+    }
+    for (int64_t g = 0; g < T; ++g)
+        for (int32_t k = 0; k < K; ++k) {
+            int32_t e = topk_idx[g * K + k];
+            if (e < 0 || e >= E) { expert_slot[g * K + k] = -1; continue; }
+            int32_t row = expert_offset[e] + seen[e];
+            seen[e] += 1;
+            expert_slot[g * K + k] = row;
+            expert_src_row[row] = recv_slot[g * R + e / m];
+            if (topk_w && expert_weight) expert_weight[row] = topk_w[g * K + k];
+        }
+    free(seen);
+    return err;
+}
+
 /* -------------------------------------------------------------- dispatch */
 
 int moe_ref_dispatch_bf16(const uint16_t* x, int32_t T, int32_t H, int32_t R,

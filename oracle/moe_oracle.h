@@ -75,6 +75,32 @@ int moe_ref_layout(const int32_t* topk_idx, const float* topk_w,
                    int32_t* expert_slot, int32_t* recv_src_token,
                    int32_t* expert_src_row, float* expert_weight);
 
+/* Multi-source receive layout: the single-GPU stand-in for the exchange in
+ * which every source rank sends its tokens to the ranks of their experts and
+ * every destination rank receives from all sources ("Inside the Nebius +
+ * PyTorch DeepSeek V3 recipe", section "Mixture-of-experts and wide expert
+ * parallelism").  S sources hold Ts tokens each; token g of the concatenated
+ * routing topk_idx [T,K], T = S*Ts, belongs to source g / Ts.  Destination r
+ * owns the receive region [r*T, (r+1)*T) (its worst case: every token of
+ * every source); the tokens reaching r fill it from its start in (source,
+ * token) order, which is ascending g.  Outputs:
+ *   recv_slot[g,r]            r*T + #{g' < g : g' has a valid expert on r}, or -1
+ *   tokens_per_rank[r]        rows used in region r
+ *   rank_offset[R+1]          r*T (region starts); rank_offset[R] = R*T
+ *   recv_source_offset[R,S+1] #{g < s*Ts : g reaches r}: source s's rows in
+ *                             region r are [offset[r,s], offset[r,s+1]) from
+ *                             the region start; offset[r,S] = tokens_per_rank[r]
+ *   recv_src_token[R*T]       g of each used row, -1 in every region's tail
+ * and the expert-major outputs exactly as moe_ref_layout defines them over
+ * the T tokens (expert_src_row maps through this recv_slot). */
+int moe_ref_layout_sources(const int32_t* topk_idx, const float* topk_w,
+                           int32_t S, int32_t Ts, int32_t K, int32_t E, int32_t R,
+                           int32_t* tokens_per_expert, int32_t* expert_offset,
+                           int32_t* tokens_per_rank, int32_t* rank_offset,
+                           int32_t* recv_source_offset, int32_t* recv_slot,
+                           int32_t* expert_slot, int32_t* recv_src_token,
+                           int32_t* expert_src_row, float* expert_weight);
+
 /* bf16 dispatch: recv_x[recv_slot[t,r], :] = x[t, :] for every recv_slot >= 0.
  * x [T,H] and recv_x [capacity,H] hold bf16 bit patterns. */
 int moe_ref_dispatch_bf16(const uint16_t* x, int32_t T, int32_t H, int32_t R,

@@ -13,6 +13,7 @@ import oracle
 import test_oracle_codecs as C
 import test_oracle_dispatch_combine as D
 import test_oracle_layout as LY
+import test_oracle_sources as SRC
 
 HERE = os.path.dirname(os.path.abspath(oracle.__file__))
 
@@ -48,6 +49,16 @@ MUTANTS = [
      "tokens_per_expert[e] += 1;", "tokens_per_expert[e] = 1;"),
     ("layout orders receive rows by token only",
      "slot = recv_expert_offset[p] + seen[p];", "slot = recv_expert_offset[r * m] + seen[r * m];"),
+    ("multi-source regions sized by one source",
+     "slot = (int32_t)((int64_t)r * T + used);", "slot = (int32_t)((int64_t)r * Ts + used);"),
+    ("multi-source walks each source's tokens backwards",
+     "for (int32_t t = 0; t < Ts; ++t) {\n                int64_t g = (int64_t)s * Ts + t;",
+     "for (int32_t t = Ts - 1; t >= 0; --t) {\n                int64_t g = (int64_t)s * Ts + t;"),
+    ("multi-source never writes the per-source offsets",
+     "recv_source_offset[(int64_t)r * (S + 1) + s] = used;\n            for",
+     "for"),
+    ("multi-source leaves region tails uncleared",
+     "for (int64_t i = 0; i < (int64_t)R * T; ++i) recv_src_token[i] = -1;", ""),
 ]
 
 
@@ -62,6 +73,8 @@ def _pins():
         ("bf16 exact", lambda: C.test_bf16_encode_vs_exact_rounding(o)),
         ("layout golden", lambda: LY.test_layout_worked_example(o)),
         ("layout brute force", lambda: LY.test_layout_vs_brute_force(o, 13, 4, 8, 2, 0.2, True, 3)),
+        ("sources golden", lambda: SRC.test_sources_worked_example(o)),
+        ("sources by sorting", lambda: SRC.test_sources_vs_sorting(o, 3, 20, 4, 16, 4, 0.2, True, 1)),
         ("fp8 exact pipeline", lambda: D.test_dispatch_fp8_vs_exact_pipeline(o)),
         ("combine exact chain", lambda: D.test_combine_vs_exact_fma_chain(o)),
         ("combine ascending k", D.test_combine_sums_in_ascending_k),
