@@ -319,6 +319,38 @@ def run_ours(args, rank, world, local_rank):
     lld = [e[0].elapsed_time(e[1]) for e in evl]
     llc = [e[1].elapsed_time(e[2]) for e in evl]
     ll_bytes = 2 * T_ll * H + 2 * H * T_ll * K + 4 * T_ll * K    # rows read, one row per entry written
+    del recv_ll, grad_recv, grad_y, recv8, scales8, recvmx, scalesmx
+
+    # multi-source receive: all eight ranks' tokens of this shape at once (S = 8
+    # sources of T tokens, one region of 8T rows per destination rank)
+    S_ms = 8
+    inp_ms = make_inputs(wl.scaled(S_ms * T), seed=1000 + rank, with_y=False)
+    L_ms = ep.Layout(S_ms * T, K, E, R, device=dev, sources=S_ms)
+    x_ms, idx_ms, w_ms = inp_ms.x.to(dev), inp_ms.topk_idx.to(dev), inp_ms.topk_w.to(dev)
+    gen = torch.Generator(device=dev).manual_seed(77 + rank)
+    y_ms = torch.randn(S_ms * T * K, H, device=dev, generator=gen).to(torch.bfloat16)
+    recv_ms, _ = ep.alloc_recv(L_ms, H, False, device=dev)
+    out_ms = torch.empty(S_ms * T, H, dtype=torch.bfloat16, device=dev)
+    evm = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(max(args.steps // 10, 3))]
+    for e in evm:
+        flush()
+        e[0].record(stream)
+        ep.moe_dispatch_layout(idx_ms, w_ms, E, R, L_ms, stream)
+        e[1].record(stream)
+        ep.moe_dispatch(x_ms, L_ms, False, recv_ms, None, stream)
+        e[2].record(stream)
+        ep.moe_combine(y_ms, L_ms, w_ms, out_ms, stream)
+        e[3].record(stream)
+    torch.cuda.synchronize(dev)
+    st, flags = ep.moe_layout_read_status(L_ms, stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the multi-source leg")
+    msl = statistics.mean(e[0].elapsed_time(e[1]) for e in evm)
+    msd = statistics.mean(e[1].elapsed_time(e[2]) for e in evm)
+    msc = statistics.mean(e[2].elapsed_time(e[3]) for e in evm)
+    ab_ms = algorithmic_bytes(S_ms * T, H, E, R, K, int(L_ms.tokens_per_rank.sum().item()),
+                              int(L_ms.expert_offset[E].item()), L_ms.capacity)
+    del x_ms, y_ms, recv_ms, out_ms, L_ms
 
     e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if rank == 0 else None
 
@@ -369,6 +401,15 @@ def run_ours(args, rank, world, local_rank):
             "combine_backward": {"us": round(statistics.mean(cbwd) * 1e3, 2), "bytes": ab["combine_backward"],
                                  "GB/s": round(gbps(ab["combine_backward"], statistics.mean(cbwd)), 1),
                                  "frac": round(gbps(ab["combine_backward"], statistics.mean(cbwd)) / peak, 4)},
+            "multi_source_S8": {
+                "note": f"8 sources x {T} tokens, one region of {8 * T} rows per destination rank",
+                "layout_us": round(msl * 1e3, 2),
+                "dispatch_bf16": {"us": round(msd * 1e3, 2), "bytes": ab_ms["dispatch"],
+                                  "GB/s": round(gbps(ab_ms["dispatch"], msd), 1),
+                                  "frac": round(gbps(ab_ms["dispatch"], msd) / peak, 4)},
+                "combine": {"us": round(msc * 1e3, 2), "bytes": ab_ms["combine"],
+                            "GB/s": round(gbps(ab_ms["combine"], msc), 1),
+                            "frac": round(gbps(ab_ms["combine"], msc) / peak, 4)}},
         },
         "roofline": {"bound": "hbm", "kernel": "combine_kernel<8>", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),

@@ -54,8 +54,10 @@ struct Carve {
     }
 };
 
+// num_sources == 0: single-source layout (recv_expert_offset [E+1]);
+// S >= 1: multi-source layout (recv_source_offset [R, S+1] instead).
 size_t carve_layout(moe_layout* L, void* mem, int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity,
-                    int32_t tile_tokens, int32_t num_tiles) {
+                    int32_t num_tiles, int32_t num_sources) {
     Carve c(mem);
     moe_layout tmp;
     moe_layout* o = L ? L : &tmp;
@@ -63,7 +65,13 @@ size_t carve_layout(moe_layout* L, void* mem, int32_t T, int32_t K, int32_t E, i
     o->expert_offset = c.take<int32_t>(E + 1);
     o->tokens_per_rank = c.take<int32_t>(R);
     o->rank_offset = c.take<int32_t>(R + 1);
-    o->recv_expert_offset = c.take<int32_t>(E + 1);
+    if (num_sources == 0) {
+        o->recv_expert_offset = c.take<int32_t>(E + 1);
+        o->recv_source_offset = nullptr;
+    } else {
+        o->recv_expert_offset = nullptr;
+        o->recv_source_offset = c.take<int32_t>(static_cast<size_t>(R) * (num_sources + 1));
+    }
     o->recv_slot = c.take<int32_t>(static_cast<size_t>(T) * R);
     o->expert_slot = c.take<int32_t>(static_cast<size_t>(T) * K);
     o->recv_src_token = c.take<int32_t>(static_cast<size_t>(capacity));
@@ -73,11 +81,19 @@ size_t carve_layout(moe_layout* L, void* mem, int32_t T, int32_t K, int32_t E, i
     const size_t ws_bytes = moe::layout_workspace_bytes(T, K, E, num_tiles);
     o->workspace = c.take<char>(ws_bytes);
     o->workspace_bytes = ws_bytes;
-    (void)tile_tokens;
     return c.off;
 }
 
 moe_status from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+// The fields that tell the two layout kinds apart are consistent.
+bool layout_mode_ok(const moe_layout* L) {
+    if (L->num_sources == 0) return L->recv_expert_offset != nullptr;
+    if (L->num_sources < 0 || L->num_sources > MOE_MAX_SOURCES || L->source_tokens < 0) return false;
+    return L->recv_source_offset != nullptr &&
+           static_cast<int64_t>(L->num_sources) * L->source_tokens == L->T &&
+           L->capacity == static_cast<int64_t>(L->T) * L->R;
+}
 
 uint64_t timeout_of(const moe_tuning* t) {
     return (t && t->wait_timeout_ns) ? t->wait_timeout_ns : moe::kDefaultWaitNs;
@@ -90,7 +106,7 @@ extern "C" {
 size_t moe_layout_bytes(int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity) {
     if (!sizes_ok(T, K, E, R) || capacity < 0) return 0;
     const int32_t tt = moe::default_tile_tokens(T, K);
-    return carve_layout(nullptr, nullptr, T, K, E, R, capacity, tt, num_tiles_for(T, tt));
+    return carve_layout(nullptr, nullptr, T, K, E, R, capacity, num_tiles_for(T, tt), 0);
 }
 
 moe_status moe_layout_init(moe_layout* L, int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity,
@@ -108,7 +124,43 @@ moe_status moe_layout_init(moe_layout* L, int32_t T, int32_t K, int32_t E, int32
     L->capacity = capacity;
     L->tile_tokens = moe::default_tile_tokens(T, K);
     L->num_tiles = num_tiles_for(T, L->tile_tokens);
-    carve_layout(L, device_mem, T, K, E, R, capacity, L->tile_tokens, L->num_tiles);
+    L->num_sources = 0;
+    L->source_tokens = T;
+    carve_layout(L, device_mem, T, K, E, R, capacity, L->num_tiles, 0);
+    return MOE_OK;
+}
+
+size_t moe_layout_sources_bytes(int32_t S, int32_t source_tokens, int32_t K, int32_t E, int32_t R) {
+    if (S < 1 || S > MOE_MAX_SOURCES || source_tokens < 0) return 0;
+    const int64_t T = static_cast<int64_t>(S) * source_tokens;
+    if (T > INT32_MAX || !sizes_ok(static_cast<int32_t>(T), K, E, R)) return 0;
+    const int64_t cap = T * R;
+    if (cap > INT32_MAX) return 0;
+    const int32_t t32 = static_cast<int32_t>(T);
+    const int32_t tt = moe::default_tile_tokens(t32, K);
+    return carve_layout(nullptr, nullptr, t32, K, E, R, cap, num_tiles_for(t32, tt), S);
+}
+
+moe_status moe_layout_init_sources(moe_layout* L, int32_t S, int32_t source_tokens, int32_t K, int32_t E, int32_t R,
+                                   void* device_mem, size_t bytes) {
+    if (!L || !device_mem || S < 1 || source_tokens < 0) return MOE_ERR_INVALID_ARG;
+    if (S > MOE_MAX_SOURCES) return MOE_ERR_UNSUPPORTED;
+    const int64_t T = static_cast<int64_t>(S) * source_tokens;
+    if (T > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    const int32_t t32 = static_cast<int32_t>(T);
+    if (!sizes_ok(t32, K, E, R)) return MOE_ERR_INVALID_ARG;
+    if (!sizes_supported(K, E, R)) return MOE_ERR_UNSUPPORTED;
+    if (T * R > INT32_MAX || T * K > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(device_mem) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (bytes < moe_layout_sources_bytes(S, source_tokens, K, E, R)) return MOE_ERR_INVALID_ARG;
+    std::memset(L, 0, sizeof(*L));
+    L->T = t32; L->K = K; L->E = E; L->R = R;
+    L->capacity = T * R;
+    L->tile_tokens = moe::default_tile_tokens(t32, K);
+    L->num_tiles = num_tiles_for(t32, L->tile_tokens);
+    L->num_sources = S;
+    L->source_tokens = source_tokens;
+    carve_layout(L, device_mem, t32, K, E, R, L->capacity, L->num_tiles, S);
     return MOE_OK;
 }
 
@@ -116,6 +168,7 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w, int
                                int32_t num_ranks, moe_layout* L, void* stream, const moe_tuning* tuning) {
     if (!L || !L->workspace || !L->status) return MOE_ERR_INVALID_ARG;
     if (num_experts != L->E || num_ranks != L->R) return MOE_ERR_INVALID_ARG;
+    if (!layout_mode_ok(L)) return MOE_ERR_INVALID_ARG;
     if (L->T > 0 && !topk_idx) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_layout(topk_idx, topk_w, L, static_cast<cudaStream_t>(stream), timeout_of(tuning),
                                         tuning ? tuning->debug_flags : 0u));

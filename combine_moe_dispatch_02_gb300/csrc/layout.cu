@@ -12,8 +12,9 @@
 //  1. layout_scan_kernel: one CTA per tile of about 2048 (t,k) entries.  Tile
 //     ids come from an atomic ticket, so a CTA only ever waits on tiles that
 //     running CTAs have claimed.  Per tile: warp-aggregated, order-preserving
-//     ranks of every entry among the entries of its expert (match_any + popc
-//     inside a warp, per-warp histograms in shared memory, an exclusive scan
+//     ranks of every entry among the entries of its expert (peer masks from
+//     one ballot per id bit + popc inside a warp, per-warp histograms in
+//     shared memory, an exclusive scan
 //     across warps) and, in the same pass, among the "primary" entries; then
 //     a decoupled look-back over the 2E-wide count vectors of earlier tiles
 //     (one warp inspects 32 predecessors at a time; the vectors are summed
@@ -25,6 +26,13 @@
 //     recv_slot, expert_slot, recv_src_token, expert_src_row and
 //     expert_weight with coalesced row writes, plus the tails past the last
 //     used row.
+// The multi-source layout (S source ranks, one worst-case region per
+// destination, rows in (source, token) order) uses the same two kernels with
+// the primary pairs counted per destination rank instead of per primary
+// expert, and a third, layout_source_offsets_kernel, that reads each source's
+// first row per region off the sorted regions by binary search.
+#include <algorithm>
+
 #include "moe_common.cuh"
 
 namespace moe {
@@ -96,6 +104,11 @@ __device__ uint32_t wait_tile_flag(const uint32_t* flag, uint32_t gen, const uin
     }
 }
 
+// SRC = false: primary pairs are counted per primary expert (the single-source
+// layout, rows grouped by expert inside each rank).  SRC = true: they are
+// counted per destination rank in the column of the rank's first expert (the
+// multi-source layout, rows in token order inside each rank's region).
+template <bool SRC>
 __global__ void __launch_bounds__(kLayoutThreads, 1)
 layout_scan_kernel(ScanArgs a) {
     extern __shared__ __align__(16) int32_t smem[];
@@ -153,6 +166,7 @@ layout_scan_kernel(ScanArgs a) {
     int32_t key[kMaxChunksPerWarp];
     bool prim[kMaxChunksPerWarp];
     uint32_t peers[kMaxChunksPerWarp];
+    uint32_t rpeers[kMaxChunksPerWarp];     // SRC: lanes with the same rank
 #pragma unroll
     for (int c = 0; c < kMaxChunksPerWarp; ++c) {
         const int i = warp * seg + c * 32 + lane;
@@ -164,6 +178,7 @@ layout_scan_kernel(ScanArgs a) {
         }
         peers[c] = __ballot_sync(0xffffffffu, key[c] >= 0);
         if (key[c] < 0) peers[c] = ~peers[c];
+        rpeers[c] = peers[c];
     }
     for (int b = 0; b < nbits; ++b) {
 #pragma unroll
@@ -173,6 +188,17 @@ layout_scan_kernel(ScanArgs a) {
             peers[c] &= bit ? bb : ~bb;
         }
     }
+    if constexpr (SRC) {
+        const int rbits = 32 - __clz(max(a.R - 1, 1));
+        for (int b = 16; b < 16 + rbits; ++b) {
+#pragma unroll
+            for (int c = 0; c < kMaxChunksPerWarp; ++c) {
+                const bool bit = (key[c] >> b) & 1;
+                const uint32_t bb = __ballot_sync(0xffffffffu, bit);
+                rpeers[c] &= bit ? bb : ~bb;
+            }
+        }
+    }
     // 2b. per-warp histogram updates, chunk by chunk
     const uint32_t lt = lanemask_lt();
 #pragma unroll
@@ -180,13 +206,18 @@ layout_scan_kernel(ScanArgs a) {
         lr_e[c] = -1; lr_p[c] = -1; ent_e[c] = -1;
         if (c * 32 >= seg) continue;            // warp-uniform
         const int e = key[c] >= 0 ? (key[c] & 0xffff) : -1;
-        const uint32_t pmask = __ballot_sync(0xffffffffu, prim[c]) & peers[c];
+        // primary counter column: the expert's own, or (SRC) its rank's first expert's
+        const int pcol = a.E + (SRC ? (key[c] >> 16) * a.m : e);
+        const uint32_t pmask = __ballot_sync(0xffffffffu, prim[c]) & (SRC ? rpeers[c] : peers[c]);
         int base_e = 0, base_p = 0;
-        if (e >= 0) { base_e = my_hist[e]; base_p = my_hist[a.E + e]; }
+        if (e >= 0) { base_e = my_hist[e]; base_p = my_hist[pcol]; }
         __syncwarp();
         if (e >= 0 && (peers[c] & lt) == 0) {    // lowest lane of its group updates
             my_hist[e] = base_e + __popc(peers[c]);
-            my_hist[a.E + e] = base_p + __popc(pmask);
+            if constexpr (!SRC) my_hist[pcol] = base_p + __popc(pmask);
+        }
+        if constexpr (SRC) {
+            if (prim[c] && (pmask & lt) == 0) my_hist[pcol] = base_p + __popc(pmask);
         }
         __syncwarp();
         if (e >= 0) {
@@ -304,8 +335,9 @@ layout_scan_kernel(ScanArgs a) {
         if (ent_e[c] < 0) continue;
         const int e = ent_e[c];
         const int64_t gi = static_cast<int64_t>(t0) * a.K + warp * seg + c * 32 + lane;
+        const int pcol = a.E + (SRC ? s_rank[e] * a.m : e);
         a.ws.erank[gi] = s_prefix[e] + my_hist[e] + lr_e[c];
-        a.ws.prank[gi] = lr_p[c] >= 0 ? s_prefix[a.E + e] + my_hist[a.E + e] + lr_p[c] : -1;
+        a.ws.prank[gi] = lr_p[c] >= 0 ? s_prefix[pcol] + my_hist[pcol] + lr_p[c] : -1;
     }
 }
 
@@ -356,6 +388,7 @@ struct FinalArgs {
     const int32_t* topk_idx;
     const float* topk_w;
     int32_t T, K, E, R, m;
+    int32_t src_order;          // multi-source layout: region r*T per destination
     int64_t capacity;
     int32_t num_tiles;
     LayoutWs ws;
@@ -415,8 +448,10 @@ layout_finalize_kernel(FinalArgs a) {
             const int64_t v = static_cast<int64_t>(s_eoff[e]) + s_er[i];
             if (v >= 0 && v < n_valid) es = static_cast<int32_t>(v); else bad = true;
             if (s_pr[i] >= 0) {
-                const int64_t rs = static_cast<int64_t>(s_poff[e]) + s_pr[i];
-                if (rs >= 0 && rs < n_pairs) {
+                const int64_t rs = a.src_order ? static_cast<int64_t>(s_rank[e]) * a.T + s_pr[i]
+                                               : static_cast<int64_t>(s_poff[e]) + s_pr[i];
+                const bool in_range = a.src_order ? (s_pr[i] < a.T && rs < a.capacity) : (rs >= 0 && rs < n_pairs);
+                if (in_range) {
                     s_rs[tl * a.R + s_rank[e]] = static_cast<int32_t>(rs);
                     a.recv_src_token[rs] = static_cast<int32_t>(t0 + tl);
                 } else {
@@ -441,7 +476,17 @@ layout_finalize_kernel(FinalArgs a) {
     // tails past the last used rows, spread over all blocks
     const int64_t gtid = static_cast<int64_t>(blockIdx.x) * kFinalizeThreads + tid;
     const int64_t gstride = static_cast<int64_t>(gridDim.x) * kFinalizeThreads;
-    for (int64_t i = n_pairs + gtid; i < a.capacity; i += gstride) a.recv_src_token[i] = -1;
+    if (a.src_order) {
+        // the unused tail of every destination region
+        for (int r = 0; r < a.R; ++r) {
+            const int64_t used = min(max(static_cast<int64_t>(s_poff[(r + 1) * a.m] - s_poff[r * a.m]), int64_t{0}),
+                                     static_cast<int64_t>(a.T));
+            int32_t* region = a.recv_src_token + static_cast<int64_t>(r) * a.T;
+            for (int64_t i = used + gtid; i < a.T; i += gstride) region[i] = -1;
+        }
+    } else {
+        for (int64_t i = n_pairs + gtid; i < a.capacity; i += gstride) a.recv_src_token[i] = -1;
+    }
     for (int64_t i = n_valid + gtid; i < n_entries; i += gstride) {
         a.expert_src_row[i] = -1;
         a.expert_weight[i] = 0.0f;
@@ -449,11 +494,11 @@ layout_finalize_kernel(FinalArgs a) {
     if (blockIdx.x == 0) {
         for (int e = tid; e <= a.E; e += kFinalizeThreads) {
             a.expert_offset[e] = s_eoff[e];
-            a.recv_expert_offset[e] = s_poff[e];
+            if (!a.src_order) a.recv_expert_offset[e] = s_poff[e];
             if (e < a.E) a.tokens_per_expert[e] = s_eoff[e + 1] - s_eoff[e];
         }
         for (int r = tid; r <= a.R; r += kFinalizeThreads) {
-            a.rank_offset[r] = s_poff[r * a.m];
+            a.rank_offset[r] = a.src_order ? r * a.T : s_poff[r * a.m];
             if (r < a.R) a.tokens_per_rank[r] = s_poff[(r + 1) * a.m] - s_poff[r * a.m];
         }
         if (tid == 0) {
@@ -465,8 +510,38 @@ layout_finalize_kernel(FinalArgs a) {
             a.ws.hdr->epoch = (a.ws.hdr->epoch + 1u) % kGenMask;
         }
     }
-    if (s_poff[a.E] > a.capacity) bad = true;
+    if (!a.src_order && s_poff[a.E] > a.capacity) bad = true;
     if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+}
+
+// Multi-source layout: per destination r and source s, the first row of
+// region r holding a token of source s or later.  Each region's used rows
+// hold ascending token ids, so this is a lower bound of s * Ts in them.
+struct SourceOffsetArgs {
+    const int32_t* recv_src_token;
+    const int32_t* tokens_per_rank;
+    int32_t* recv_source_offset;     // [R, S+1]
+    int32_t T, R, S, Ts;
+};
+
+__global__ void __launch_bounds__(256)
+layout_source_offsets_kernel(SourceOffsetArgs a) {
+    pdl_wait();
+    pdl_trigger();
+    const int64_t n = static_cast<int64_t>(a.R) * (a.S + 1);
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int r = static_cast<int>(i / (a.S + 1));
+        const int s = static_cast<int>(i - static_cast<int64_t>(r) * (a.S + 1));
+        const int32_t* rows = a.recv_src_token + static_cast<int64_t>(r) * a.T;
+        const int32_t target = s * a.Ts;           // <= T
+        int lo = 0, hi = min(max(a.tokens_per_rank[r], 0), a.T);
+        while (lo < hi) {                          // at most 32 steps
+            const int mid = lo + (hi - lo) / 2;
+            if (rows[mid] < target) lo = mid + 1; else hi = mid;
+        }
+        a.recv_source_offset[i] = lo;
+    }
 }
 
 }  // namespace
@@ -515,17 +590,22 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.tile_tokens = L->tile_tokens; sa.num_tiles = L->num_tiles;
     sa.ws = ws; sa.status = L->status;
     sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
+    const bool src = L->num_sources > 0;
     const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
                                             static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
-    cudaError_t err = cudaFuncSetAttribute(layout_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    const void* scan_fn = src ? reinterpret_cast<const void*>(layout_scan_kernel<true>)
+                              : reinterpret_cast<const void*>(layout_scan_kernel<false>);
+    cudaError_t err = cudaFuncSetAttribute(scan_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem1));
     if (err != cudaSuccess) return err;
-    err = launch_pdl(layout_scan_kernel, dim3(L->num_tiles), dim3(kLayoutThreads), smem1, stream, sa);
+    err = src ? launch_pdl(layout_scan_kernel<true>, dim3(L->num_tiles), dim3(kLayoutThreads), smem1, stream, sa)
+              : launch_pdl(layout_scan_kernel<false>, dim3(L->num_tiles), dim3(kLayoutThreads), smem1, stream, sa);
     if (err != cudaSuccess) return err;
 
     FinalArgs fa;
     fa.topk_idx = topk_idx; fa.topk_w = topk_w;
     fa.T = L->T; fa.K = L->K; fa.E = L->E; fa.R = L->R; fa.m = L->E / L->R;
+    fa.src_order = src ? 1 : 0;
     fa.capacity = L->capacity; fa.num_tiles = L->num_tiles; fa.ws = ws; fa.status = L->status;
     fa.tokens_per_expert = L->tokens_per_expert;
     fa.expert_offset = L->expert_offset; fa.recv_expert_offset = L->recv_expert_offset;
@@ -540,8 +620,18 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     err = cudaFuncSetAttribute(layout_finalize_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                static_cast<int>(smem2));
     if (err != cudaSuccess) return err;
-    return launch_pdl(layout_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFinalizeThreads), smem2,
-                      stream, fa);
+    err = launch_pdl(layout_finalize_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kFinalizeThreads), smem2,
+                     stream, fa);
+    if (err != cudaSuccess || !src) return err;
+
+    SourceOffsetArgs oa;
+    oa.recv_src_token = L->recv_src_token;
+    oa.tokens_per_rank = L->tokens_per_rank;
+    oa.recv_source_offset = L->recv_source_offset;
+    oa.T = L->T; oa.R = L->R; oa.S = L->num_sources; oa.Ts = L->source_tokens;
+    const int64_t n = static_cast<int64_t>(L->R) * (L->num_sources + 1);
+    const unsigned g3 = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 1024));
+    return launch_pdl(layout_source_offsets_kernel, dim3(g3), dim3(256), 0, stream, oa);
 }
 
 }  // namespace moe

@@ -55,9 +55,16 @@ extern "C" moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, const
     if (static_cast<int64_t>(T) * K > INT32_MAX || static_cast<int64_t>(T) * R > INT32_MAX) return MOE_ERR_UNSUPPORTED;
     if (T > 0 && !topk_idx) return MOE_ERR_INVALID_ARG;
     if (!L->tokens_per_expert || !L->expert_offset || !L->tokens_per_rank || !L->rank_offset ||
-        !L->recv_expert_offset || !L->recv_slot || !L->expert_slot || !L->recv_src_token || !L->expert_src_row ||
+        !L->recv_slot || !L->expert_slot || !L->recv_src_token || !L->expert_src_row ||
         !L->expert_weight || !L->status)
         return MOE_ERR_INVALID_ARG;
+    if (L->num_sources == 0) {
+        if (!L->recv_expert_offset) return MOE_ERR_INVALID_ARG;
+    } else if (L->num_sources < 0 || L->num_sources > MOE_MAX_SOURCES || L->source_tokens < 0 ||
+               static_cast<int64_t>(L->num_sources) * L->source_tokens != T ||
+               L->capacity != static_cast<int64_t>(T) * R || !L->recv_source_offset) {
+        return MOE_ERR_INVALID_ARG;
+    }
 
     moe_layout tmp = *L;
     tmp.tile_tokens = moe::default_tile_tokens(T, K);

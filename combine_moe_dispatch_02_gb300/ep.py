@@ -38,12 +38,14 @@ MOE_FORMAT_BF16 = 0
 MOE_FORMAT_FP8 = 1
 MOE_FORMAT_MXFP8 = 2
 
-EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
+EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_layout_sources_bytes", "moe_layout_init_sources",
+            "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
             "moe_dispatch", "moe_combine", "moe_dispatch_backward", "moe_combine_backward",
             "moe_ll_dispatch", "moe_ll_combine",
             "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
 
 MOE_NOALLOC_SCRATCH_BYTES = 8 << 20
+MOE_MAX_SOURCES = 1024
 
 
 class moe_layout(ctypes.Structure):
@@ -51,11 +53,13 @@ class moe_layout(ctypes.Structure):
         ("T", ctypes.c_int32), ("K", ctypes.c_int32), ("E", ctypes.c_int32), ("R", ctypes.c_int32),
         ("capacity", ctypes.c_int64),
         ("tile_tokens", ctypes.c_int32), ("num_tiles", ctypes.c_int32),
+        ("num_sources", ctypes.c_int32), ("source_tokens", ctypes.c_int32),
         ("tokens_per_expert", ctypes.c_void_p), ("expert_offset", ctypes.c_void_p),
         ("tokens_per_rank", ctypes.c_void_p), ("rank_offset", ctypes.c_void_p),
         ("recv_expert_offset", ctypes.c_void_p), ("recv_slot", ctypes.c_void_p),
         ("expert_slot", ctypes.c_void_p), ("recv_src_token", ctypes.c_void_p),
         ("expert_src_row", ctypes.c_void_p), ("expert_weight", ctypes.c_void_p),
+        ("recv_source_offset", ctypes.c_void_p),
         ("status", ctypes.c_void_p), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
     ]
 
@@ -88,6 +92,11 @@ def lib() -> ctypes.CDLL:
         L.moe_layout_bytes.argtypes = [i32, i32, i32, i32, i64]
         L.moe_layout_init.restype = ctypes.c_int
         L.moe_layout_init.argtypes = [ctypes.POINTER(moe_layout), i32, i32, i32, i32, i64, P, ctypes.c_size_t]
+        L.moe_layout_sources_bytes.restype = ctypes.c_size_t
+        L.moe_layout_sources_bytes.argtypes = [i32, i32, i32, i32, i32]
+        L.moe_layout_init_sources.restype = ctypes.c_int
+        L.moe_layout_init_sources.argtypes = [ctypes.POINTER(moe_layout), i32, i32, i32, i32, i32, P,
+                                              ctypes.c_size_t]
         L.moe_dispatch_layout.restype = ctypes.c_int
         L.moe_dispatch_layout.argtypes = [P, P, i32, i32, ctypes.POINTER(moe_layout), P, ctypes.POINTER(moe_tuning)]
         L.moe_dispatch_layout_noalloc.restype = ctypes.c_int
@@ -145,25 +154,43 @@ def moe_layout_bytes(T: int, K: int, E: int, R: int, capacity: int) -> int:
     return int(lib().moe_layout_bytes(T, K, E, R, capacity))
 
 
+def moe_layout_sources_bytes(S: int, source_tokens: int, K: int, E: int, R: int) -> int:
+    return int(lib().moe_layout_sources_bytes(S, source_tokens, K, E, R))
+
+
 class Layout:
     """Device memory and C struct of one routing layout.
 
     The arrays are views of one zero-initialised uint8 device buffer carved by
-    ``moe_layout_init``; the buffer stays alive as long as this object."""
+    ``moe_layout_init`` (or, with ``sources=S``, by ``moe_layout_init_sources``:
+    T = S * Ts tokens from S source ranks, capacity R * T); the buffer stays
+    alive as long as this object."""
 
     def __init__(self, T: int, K: int, E: int, R: int, capacity: int | None = None,
-                 device: torch.device | str = "cuda"):
-        if capacity is None:
-            capacity = T * min(K, R)
-        nbytes = moe_layout_bytes(T, K, E, R, capacity)
+                 device: torch.device | str = "cuda", sources: int = 0):
+        self.S = sources
+        if sources:
+            if capacity is not None or T % sources:
+                raise MoeError(MOE_ERR_INVALID_ARG, "multi-source layout: T = S * Ts, capacity R * T")
+            capacity = R * T
+            nbytes = moe_layout_sources_bytes(sources, T // sources, K, E, R)
+        else:
+            if capacity is None:
+                capacity = T * min(K, R)
+            nbytes = moe_layout_bytes(T, K, E, R, capacity)
         if nbytes == 0:
             raise MoeError(MOE_ERR_INVALID_ARG, "moe_layout_bytes")
         self.buf = torch.zeros(nbytes + 256, dtype=torch.uint8, device=device)
         base = self.buf.data_ptr()
         self._off0 = (-base) % 256                      # 256-byte aligned start
         self.c = moe_layout()
-        _check(lib().moe_layout_init(ctypes.byref(self.c), T, K, E, R, capacity,
-                                     ctypes.c_void_p(base + self._off0), nbytes), "moe_layout_init")
+        if sources:
+            _check(lib().moe_layout_init_sources(ctypes.byref(self.c), sources, T // sources, K, E, R,
+                                                 ctypes.c_void_p(base + self._off0), nbytes),
+                   "moe_layout_init_sources")
+        else:
+            _check(lib().moe_layout_init(ctypes.byref(self.c), T, K, E, R, capacity,
+                                         ctypes.c_void_p(base + self._off0), nbytes), "moe_layout_init")
         self.T, self.K, self.E, self.R, self.capacity = T, K, E, R, capacity
 
     def _view(self, field: str, count: int, dtype=torch.int32) -> torch.Tensor:
@@ -181,7 +208,11 @@ class Layout:
     @property
     def rank_offset(self): return self._view("rank_offset", self.R + 1)
     @property
-    def recv_expert_offset(self): return self._view("recv_expert_offset", self.E + 1)
+    def recv_expert_offset(self):
+        return None if self.S else self._view("recv_expert_offset", self.E + 1)
+    @property
+    def recv_source_offset(self):
+        return self._view("recv_source_offset", self.R * (self.S + 1)).view(self.R, self.S + 1) if self.S else None
     @property
     def recv_slot(self): return self._view("recv_slot", self.T * self.R).view(self.T, self.R)
     @property

@@ -112,9 +112,13 @@ typedef struct moe_layout {
     int64_t capacity;
     int32_t tile_tokens;        /* tokens per scan tile, fixed at init */
     int32_t num_tiles;
+    int32_t num_sources;        /* 0: the single-source layout above; S >= 1: the
+                                   multi-source receive layout (below)          */
+    int32_t source_tokens;      /* tokens per source, T / S (T when num_sources == 0) */
     int32_t *tokens_per_expert, *expert_offset, *tokens_per_rank, *rank_offset;
     int32_t *recv_expert_offset, *recv_slot, *expert_slot, *recv_src_token, *expert_src_row;
     float   *expert_weight;
+    int32_t *recv_source_offset; /* [R, S+1], multi-source layout only; NULL otherwise */
     uint32_t *status;
     void    *workspace;         /* scan scratch, carved from the same memory */
     size_t   workspace_bytes;
@@ -131,6 +135,43 @@ size_t moe_layout_bytes(int32_t T, int32_t K, int32_t E, int32_t R, int64_t capa
  * capacity must be >= T * min(K, R). */
 moe_status moe_layout_init(moe_layout* L, int32_t T, int32_t K, int32_t E, int32_t R,
                            int64_t capacity, void* device_mem, size_t bytes);
+
+/*
+ * Multi-source receive layout: the single-GPU stand-in for the exchange in
+ * which every source rank sends its tokens to the ranks of their experts and
+ * every destination rank receives from all sources ("Inside the Nebius +
+ * PyTorch DeepSeek V3 recipe", section "Mixture-of-experts and wide expert
+ * parallelism").  S sources of Ts tokens each; token g of the concatenated
+ * routing topk_idx [T, K], T = S * Ts, belongs to source g / Ts.  Destination
+ * r owns its own receive region, rows [r*T, (r+1)*T) -- its worst case, every
+ * token of every source -- so capacity = R * T.  The tokens that reach r fill
+ * the region from its start in (source, token) order, i.e. ascending g.
+ *
+ *  recv_slot[T,R]           r*T + #{g' < g : g' has a valid expert on r}, or -1
+ *  tokens_per_rank[R]       rows used in region r
+ *  rank_offset[R+1]         r*T, the region starts; rank_offset[R] = R*T
+ *  recv_source_offset[R,S+1] #{g < s*Ts : g reaches r}: source s's rows in
+ *                           region r are [off[r,s], off[r,s+1]) counted from
+ *                           the region start; off[r,S] = tokens_per_rank[r]
+ *  recv_src_token[R*T]      g of each used row; -1 in the unused tail of every region
+ *  recv_expert_offset       NULL: the rows are not grouped by expert
+ *
+ * The expert-major outputs (tokens_per_expert, expert_offset, expert_slot,
+ * expert_src_row, expert_weight) are those of the single-source layout over
+ * all T tokens.  moe_dispatch, moe_combine, moe_dispatch_backward and
+ * moe_combine_backward take either kind of layout unchanged; the layout call
+ * adds a third kernel that reads the per-source offsets off the sorted
+ * regions.
+ */
+#define MOE_MAX_SOURCES 1024
+
+/* Bytes for moe_layout_init_sources; 0 if the sizes are invalid. */
+size_t moe_layout_sources_bytes(int32_t S, int32_t source_tokens, int32_t K, int32_t E, int32_t R);
+
+/* As moe_layout_init, for the multi-source layout (capacity R * S * Ts).
+ * 1 <= S <= MOE_MAX_SOURCES and R * S * Ts must fit in int32. */
+moe_status moe_layout_init_sources(moe_layout* L, int32_t S, int32_t source_tokens, int32_t K, int32_t E,
+                                   int32_t R, void* device_mem, size_t bytes);
 
 /* Dispatch layout: counts, prefix offsets and token<->slot maps (all fields
  * above) from topk_idx int32 [T,K] (-1 = masked) and topk_w fp32 [T,K]
@@ -164,7 +205,9 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w,
  * Fields of *L that are read: T, K, E, R, capacity (>= T * min(K, R)), the
  * ten output pointers and status, all caller-owned device memory of the sizes
  * listed above; tile_tokens, num_tiles, workspace and workspace_bytes are
- * ignored and left unchanged.  No moe_layout_init call is needed.
+ * ignored and left unchanged.  No moe_layout_init call is needed.  For the
+ * multi-source layout also num_sources and source_tokens (T = S * Ts,
+ * capacity = R * T) and recv_source_offset instead of recv_expert_offset.
  *
  * All calls share the one array, which keeps the previous call's contents;
  * each call clears the parts that must start at zero.  Calls that overlap on

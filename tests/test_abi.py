@@ -81,3 +81,49 @@ def test_status_strings(lib):
     from combine_moe_dispatch_02_gb300 import ep
     for s in range(7):
         assert ep.moe_status_string(s) and ep.moe_status_string(s) != "unknown status"
+
+
+def test_multi_source_layout_init_validation(lib):
+    from combine_moe_dispatch_02_gb300 import ep
+    S, Ts, K, E, R = 4, 100, 3, 8, 4
+    n = ep.moe_layout_sources_bytes(S, Ts, K, E, R)
+    assert n > 4 * (S * Ts * R)                                   # recv_src_token alone is R * T ints
+    assert ep.moe_layout_sources_bytes(0, Ts, K, E, R) == 0
+    assert ep.moe_layout_sources_bytes(ep.MOE_MAX_SOURCES + 1, 1, K, E, R) == 0
+    assert ep.moe_layout_sources_bytes(S, Ts, K, 6, R) == 0          # E % R != 0
+    assert ep.moe_layout_sources_bytes(1024, 1 << 20, 1, 256, 256) == 0   # R * T overflows int32
+    L = ep.moe_layout()
+    fake = ctypes.c_void_p(1 << 20)                               # never dereferenced on the host
+    init = lib.moe_layout_init_sources
+    assert init(ctypes.byref(L), S, Ts, K, E, R, fake, n) == ep.MOE_OK
+    assert (L.T, L.capacity, L.num_sources, L.source_tokens) == (S * Ts, R * S * Ts, S, Ts)
+    assert L.recv_expert_offset is None and L.recv_source_offset
+    assert init(ctypes.byref(L), S, Ts, K, E, R, fake, n - 1) == ep.MOE_ERR_INVALID_ARG
+    assert init(ctypes.byref(L), 0, Ts, K, E, R, fake, n) == ep.MOE_ERR_INVALID_ARG
+    assert init(ctypes.byref(L), S, Ts, 33, 64, R, fake, 1 << 30) == ep.MOE_ERR_UNSUPPORTED
+    # the single-source init records no sources
+    M = ep.moe_layout()
+    assert lib.moe_layout_init(ctypes.byref(M), 16, 2, 8, 4, 32, fake, ep.moe_layout_bytes(16, 2, 8, 4, 32)) == ep.MOE_OK
+    assert M.num_sources == 0 and M.source_tokens == 16 and M.recv_source_offset is None
+
+
+def test_layout_kind_fields_must_agree(lib):
+    """moe_dispatch_layout rejects a struct whose layout-kind fields disagree
+    before anything is enqueued."""
+    from combine_moe_dispatch_02_gb300 import ep
+    S, Ts, K, E, R = 2, 16, 2, 8, 4
+    L = ep.moe_layout()
+    fake = ctypes.c_void_p(1 << 20)
+    assert lib.moe_layout_init_sources(ctypes.byref(L), S, Ts, K, E, R, fake,
+                                       ep.moe_layout_sources_bytes(S, Ts, K, E, R)) == ep.MOE_OK
+    p = ctypes.c_void_p(1 << 21)
+    for field, value in (("recv_source_offset", None), ("source_tokens", Ts + 1), ("capacity", R * S * Ts - 1),
+                         ("num_sources", -1)):
+        bad = ep.moe_layout.from_buffer_copy(L)
+        setattr(bad, field, value)
+        assert lib.moe_dispatch_layout(p, p, E, R, ctypes.byref(bad), None, None) == ep.MOE_ERR_INVALID_ARG, field
+        assert lib.moe_dispatch_layout_noalloc(p, p, E, R, ctypes.byref(bad), None, None) == ep.MOE_ERR_INVALID_ARG
+    single = ep.moe_layout()
+    assert lib.moe_layout_init(ctypes.byref(single), 16, 2, 8, 4, 32, fake, ep.moe_layout_bytes(16, 2, 8, 4, 32)) == 0
+    single.recv_expert_offset = None
+    assert lib.moe_dispatch_layout(p, p, 8, 4, ctypes.byref(single), None, None) == ep.MOE_ERR_INVALID_ARG
