@@ -32,6 +32,7 @@
 // expert, and a third, layout_source_offsets_kernel, that reads each source's
 // first row per region off the sorted regions by binary search.
 #include <algorithm>
+#include <climits>
 
 #include "moe_common.cuh"
 
@@ -39,10 +40,17 @@ namespace moe {
 
 namespace {
 
+// Tiles whose (token, rank) table fits in this many ints find their primary
+// entries with one shared-memory atomicMin per entry; larger ones (many ranks)
+// compare every entry with the token's other entries.
+constexpr int kMaxPrimSlots = 16384;
+constexpr size_t kMaxSmemPerBlock = 227 * 1024;     // opt-in dynamic shared memory per block on sm_100+
+
 struct ScanArgs {
     const int32_t* topk_idx;
     int32_t T, K, E, m, R;
     int32_t tile_tokens, num_tiles;
+    int32_t prim_table;          // tile_tokens * R <= kMaxPrimSlots
     LayoutWs ws;
     uint32_t* status;
     uint64_t timeout_ns;
@@ -120,6 +128,7 @@ layout_scan_kernel(ScanArgs a) {
     int32_t* s_agg = s_prefix + W;                                    // [W]
     int4* s_part = reinterpret_cast<int4*>(s_agg + W);                // [kLayoutThreads]
     int32_t* s_rank = reinterpret_cast<int32_t*>(s_part + kLayoutThreads);   // [E]
+    int32_t* s_min = s_rank + a.E;    // [tile_tokens][R] if prim_table: min of (e << 5 | k) per (token, rank)
     __shared__ int s_tile;
     __shared__ uint32_t s_gen;
     __shared__ int s_lb_count, s_lb_final;
@@ -133,6 +142,8 @@ layout_scan_kernel(ScanArgs a) {
     }
     for (int i = tid; i < kLayoutWarps * W; i += kLayoutThreads) s_hist[i] = 0;
     for (int e = tid; e < a.E; e += kLayoutThreads) s_rank[e] = e / a.m;
+    if (a.prim_table)
+        for (int i = tid; i < a.tile_tokens * a.R; i += kLayoutThreads) s_min[i] = INT_MAX;
     __syncthreads();
     const int tile = s_tile;
     const uint32_t gen = s_gen;
@@ -143,13 +154,24 @@ layout_scan_kernel(ScanArgs a) {
     const int nt = min(a.tile_tokens, a.T - t0);
     const int n = nt * a.K;
 
-    // 1. the tile's entries as keys; ids outside [-1, E) are flagged and masked
+    // 1. the tile's entries as keys; ids outside [-1, E) are flagged and masked.
+    //    With the table, every valid entry also bids (e << 5 | k) for the
+    //    smallest id of its token on its rank (ties: the first k).
     bool bad = false;
+    const float inv_k = 1.0f / static_cast<float>(a.K);
     for (int i = tid; i < n; i += kLayoutThreads) {
         const int e = a.topk_idx[static_cast<int64_t>(t0) * a.K + i];
         int32_t key = -1;
-        if (e >= 0 && e < a.E) key = (s_rank[e] << 16) | e;
-        else if (e != -1) bad = true;
+        if (e >= 0 && e < a.E) {
+            const int r = s_rank[e];
+            key = (r << 16) | e;
+            if (a.prim_table) {
+                const int tl = div_small(i, inv_k);
+                atomicMin(&s_min[tl * a.R + r], (e << 5) | (i - tl * a.K));
+            }
+        } else if (e != -1) {
+            bad = true;
+        }
         s_key[i] = key;
     }
     if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_EXPERT_ID);
@@ -159,7 +181,6 @@ layout_scan_kernel(ScanArgs a) {
     //    same expert are found with one ballot per bit of the expert id.
     const int seg = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
     const int nbits = 32 - __clz(max(a.E - 1, 1));
-    const float inv_k = 1.0f / static_cast<float>(a.K);
     int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
     int32_t* my_hist = s_hist + warp * W;
     // 2a. keys, primary flags and peer masks of all chunks (independent work)
@@ -174,7 +195,9 @@ layout_scan_kernel(ScanArgs a) {
         prim[c] = false;
         if (key[c] >= 0) {
             const int tl = div_small(i, inv_k);
-            prim[c] = is_primary_key(s_key + tl * a.K, a.K, i - tl * a.K, key[c]);
+            const int k = i - tl * a.K;
+            prim[c] = a.prim_table ? s_min[tl * a.R + (key[c] >> 16)] == (((key[c] & 0xffff) << 5) | k)
+                                   : is_primary_key(s_key + tl * a.K, a.K, k, key[c]);
         }
         peers[c] = __ballot_sync(0xffffffffu, key[c] >= 0);
         if (key[c] < 0) peers[c] = ~peers[c];
@@ -591,8 +614,12 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.ws = ws; sa.status = L->status;
     sa.timeout_ns = timeout_ns; sa.debug_flags = debug_flags;
     const bool src = L->num_sources > 0;
-    const size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
-                                            static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
+    size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
+                                      static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
+    const size_t table_bytes = sizeof(int32_t) * static_cast<size_t>(L->tile_tokens) * L->R;
+    sa.prim_table = (static_cast<int64_t>(L->tile_tokens) * L->R <= kMaxPrimSlots &&
+                     smem1 + table_bytes <= kMaxSmemPerBlock) ? 1 : 0;
+    if (sa.prim_table) smem1 += table_bytes;
     const void* scan_fn = src ? reinterpret_cast<const void*>(layout_scan_kernel<true>)
                               : reinterpret_cast<const void*>(layout_scan_kernel<false>);
     cudaError_t err = cudaFuncSetAttribute(scan_fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
