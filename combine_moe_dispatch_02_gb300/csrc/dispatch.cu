@@ -149,7 +149,9 @@ dispatch_bf16_kernel(DispatchArgs a) {
         }
     }
     pdl_trigger();          // many waves: let the next kernel launch only as channels finish
-    bulk_wait_all();
+    // Exit once the stores have read the stages: the shared memory goes away
+    // with the CTA, while kernel completion makes the global writes visible.
+    bulk_wait_read<0>();
     const uint32_t any_bad = __ballot_sync(0xffffffffu, bad);
     const uint32_t any_tmo = __ballot_sync(0xffffffffu, timed_out);
     if (lane == 0) {
@@ -282,7 +284,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
         }
     }
     pdl_trigger();
-    if (warp == 0) bulk_wait_all();
+    if (warp == 0) bulk_wait_read<0>();     // stages read; completion publishes the writes
     if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
     if (timed_out && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
 }
@@ -417,7 +419,7 @@ dispatch_fp8_ws_kernel(DispatchArgs a) {
                 if (lane == 0) mbar_arrive(&out_empty[(k - 1) % kWsOutStages]);
             }
         }
-        bulk_wait_all();
+        bulk_wait_read<0>();                 // stages read; completion publishes the writes
         // After a timeout, loads may still be landing in the input ring: wait
         // (bounded) for the last load issued into each stage before exiting.
         for (int s = 0; s < kWsInStages && s < issued; ++s) {

@@ -44,6 +44,9 @@ namespace {
 // entries with one shared-memory atomicMin per entry; larger ones (many ranks)
 // compare every entry with the token's other entries.
 constexpr int kMaxPrimSlots = 16384;
+constexpr int kFinalizePerThread = kFinalizeTokens * MOE_MAX_TOPK / kFinalizeThreads;   // entries per thread (4)
+static_assert(kFinalizePerThread * kFinalizeThreads == kFinalizeTokens * MOE_MAX_TOPK,
+              "a finalize block's threads cover its 32 tokens' entries for every K <= MOE_MAX_TOPK");
 constexpr size_t kMaxSmemPerBlock = 227 * 1024;     // opt-in dynamic shared memory per block on sm_100+
 
 struct ScanArgs {
@@ -93,6 +96,7 @@ __device__ __forceinline__ int div_small(int i, float inv_k) {
 }
 
 constexpr uint32_t kWaitTimedOut = 4u;
+constexpr int kLookbackWindow = 32;      // predecessors one look-back step inspects (warp 0's lanes)
 
 // Wait (bounded) until a tile flag carries generation `gen`; return its state,
 // kFlagError if another CTA aborted the scan, or kWaitTimedOut.
@@ -141,6 +145,7 @@ layout_scan_kernel(ScanArgs a) {
         s_gen = (ld_relaxed_gpu(&a.ws.hdr->epoch) & kGenMask) + 1u;
     }
     for (int i = tid; i < kLayoutWarps * W; i += kLayoutThreads) s_hist[i] = 0;
+    for (int i = tid; i < W; i += kLayoutThreads) s_agg[i] = 0;
     for (int e = tid; e < a.E; e += kLayoutThreads) s_rank[e] = e / a.m;
     if (a.prim_table)
         for (int i = tid; i < a.tile_tokens * a.R; i += kLayoutThreads) s_min[i] = INT_MAX;
@@ -155,8 +160,9 @@ layout_scan_kernel(ScanArgs a) {
     const int n = nt * a.K;
 
     // 1. the tile's entries as keys; ids outside [-1, E) are flagged and masked.
-    //    With the table, every valid entry also bids (e << 5 | k) for the
-    //    smallest id of its token on its rank (ties: the first k).
+    //    Every valid entry counts itself in the tile aggregate, and, with the
+    //    table, bids (e << 5 | k) for the smallest id of its token on its rank
+    //    (ties: the first k).
     bool bad = false;
     const float inv_k = 1.0f / static_cast<float>(a.K);
     for (int i = tid; i < n; i += kLayoutThreads) {
@@ -165,6 +171,7 @@ layout_scan_kernel(ScanArgs a) {
         if (e >= 0 && e < a.E) {
             const int r = s_rank[e];
             key = (r << 16) | e;
+            atomicAdd(&s_agg[e], 1);
             if (a.prim_table) {
                 const int tl = div_small(i, inv_k);
                 atomicMin(&s_min[tl * a.R + r], (e << 5) | (i - tl * a.K));
@@ -176,18 +183,13 @@ layout_scan_kernel(ScanArgs a) {
     }
     if (__syncthreads_or(bad) && tid == 0) atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_EXPERT_ID);
 
-    // 2. order-preserving ranks inside the tile: warp w owns a contiguous
-    //    segment of 32-entry chunks and keeps its own histogram.  Lanes with the
-    //    same expert are found with one ballot per bit of the expert id.
+    // 1b. primary flags of the entries this lane ranks below (warp w owns a
+    //     contiguous segment of 32-entry chunks); primaries complete the tile
+    //     aggregate in their column: the primary expert's own or (SRC) the
+    //     first expert of the rank
     const int seg = ((n + kLayoutWarps - 1) / kLayoutWarps + 31) / 32 * 32;
-    const int nbits = 32 - __clz(max(a.E - 1, 1));
-    int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
-    int32_t* my_hist = s_hist + warp * W;
-    // 2a. keys, primary flags and peer masks of all chunks (independent work)
     int32_t key[kMaxChunksPerWarp];
     bool prim[kMaxChunksPerWarp];
-    uint32_t peers[kMaxChunksPerWarp];
-    uint32_t rpeers[kMaxChunksPerWarp];     // SRC: lanes with the same rank
 #pragma unroll
     for (int c = 0; c < kMaxChunksPerWarp; ++c) {
         const int i = warp * seg + c * 32 + lane;
@@ -198,7 +200,34 @@ layout_scan_kernel(ScanArgs a) {
             const int k = i - tl * a.K;
             prim[c] = a.prim_table ? s_min[tl * a.R + (key[c] >> 16)] == (((key[c] & 0xffff) << 5) | k)
                                    : is_primary_key(s_key + tl * a.K, a.K, k, key[c]);
+            if (prim[c]) atomicAdd(&s_agg[a.E + (SRC ? (key[c] >> 16) * a.m : (key[c] & 0xffff))], 1);
         }
+    }
+    __syncthreads();
+
+    // 1c. publish the tile aggregate now, so that successors find it on their
+    //     first look-back poll; tile 0's aggregate is its inclusive prefix
+    //     (the barrier orders every thread's stores before thread 0's fence
+    //     and release store, which publish them at GPU scope)
+    const bool stall = (a.debug_flags & MOE_DEBUG_STALL_FIRST_TILE) && tile == 0;
+    int32_t* my_vec = (tile == 0 ? a.ws.tile_incl : a.ws.tile_agg) + static_cast<int64_t>(tile) * W;
+    for (int col = tid; col < W; col += kLayoutThreads) my_vec[col] = s_agg[col];
+    __syncthreads();
+    if (tid == 0 && !stall) {
+        __threadfence();
+        st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | (tile == 0 ? kFlagPrefix : kFlagAgg));
+    }
+
+    // 2. order-preserving ranks inside the tile: each warp keeps its own
+    //    histogram.  Lanes with the same expert are found with one ballot per
+    //    bit of the expert id.
+    const int nbits = 32 - __clz(max(a.E - 1, 1));
+    int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
+    int32_t* my_hist = s_hist + warp * W;
+    uint32_t peers[kMaxChunksPerWarp];
+    uint32_t rpeers[kMaxChunksPerWarp];     // SRC: lanes with the same rank
+#pragma unroll
+    for (int c = 0; c < kMaxChunksPerWarp; ++c) {
         peers[c] = __ballot_sync(0xffffffffu, key[c] >= 0);
         if (key[c] < 0) peers[c] = ~peers[c];
         rpeers[c] = peers[c];
@@ -251,7 +280,7 @@ layout_scan_kernel(ScanArgs a) {
     }
     __syncthreads();
 
-    // 3. exclusive scan of the per-warp histograms; tile aggregate
+    // 3. exclusive scan of the per-warp histograms (each warp's base)
     for (int col = tid; col < W; col += kLayoutThreads) {
         int run = 0;
 #pragma unroll
@@ -260,26 +289,14 @@ layout_scan_kernel(ScanArgs a) {
             s_hist[w * W + col] = run;
             run += v;
         }
-        s_agg[col] = run;
         s_prefix[col] = 0;
     }
     __syncthreads();
 
-    // 4. decoupled look-back
-    const bool stall = (a.debug_flags & MOE_DEBUG_STALL_FIRST_TILE) && tile == 0;
+    // 4. decoupled look-back over the predecessors' aggregates and inclusive
+    //    prefixes
     bool failed = false;
-    if (tile == 0) {
-        for (int col = tid; col < W; col += kLayoutThreads) a.ws.tile_incl[col] = s_agg[col];
-        __threadfence();
-        __syncthreads();
-        if (tid == 0 && !stall) st_release_gpu(&a.ws.tile_flag[0], (gen << 2) | kFlagPrefix);
-    } else {
-        int32_t* my_agg = a.ws.tile_agg + static_cast<int64_t>(tile) * W;
-        for (int col = tid; col < W; col += kLayoutThreads) my_agg[col] = s_agg[col];
-        __threadfence();
-        __syncthreads();
-        if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagAgg);
-
+    if (tile > 0) {
         // the window's vectors are summed by `groups` thread groups, each taking
         // every groups-th predecessor, with 16-byte loads: one round of loads
         const int groups = max(1, min(8, kLayoutThreads / nvec));
@@ -304,7 +321,7 @@ layout_scan_kernel(ScanArgs a) {
                         s_lb_count = __ffs(pre);    // lanes 0..nearest prefix tile
                         s_lb_final = 1;
                     } else {
-                        s_lb_count = min(32, hi + 1);
+                        s_lb_count = min(kLookbackWindow, hi + 1);
                         s_lb_final = 0;
                     }
                 }
@@ -342,15 +359,9 @@ layout_scan_kernel(ScanArgs a) {
         }
         if (failed) {
             if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagError);
-        } else {
-            int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * W;
-            for (int col = tid; col < W; col += kLayoutThreads) my_incl[col] = s_prefix[col] + s_agg[col];
-            __threadfence();
-            __syncthreads();
-            if (tid == 0) st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagPrefix);
+            return;
         }
     }
-    if (failed) return;
 
     // 5. per-entry ranks including the tile prefix (prank = -1: not primary)
 #pragma unroll
@@ -361,6 +372,24 @@ layout_scan_kernel(ScanArgs a) {
         const int pcol = a.E + (SRC ? s_rank[e] * a.m : e);
         a.ws.erank[gi] = s_prefix[e] + my_hist[e] + lr_e[c];
         a.ws.prank[gi] = lr_p[c] >= 0 ? s_prefix[pcol] + my_hist[pcol] + lr_p[c] : -1;
+    }
+
+    // 6. the inclusive prefix.  The last tile's is the totals vector the
+    //    finalize pass reads (kernel completion publishes it).  Other tiles
+    //    publish theirs only when a look-back can need it: with at most 33
+    //    tiles every look-back window reaches tile 0, whose prefix is published
+    //    with its aggregate.
+    const bool flagged = a.num_tiles > kLookbackWindow + 1;
+    if (tile > 0 && (flagged || tile == a.num_tiles - 1)) {
+        int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * W;
+        for (int col = tid; col < W; col += kLayoutThreads) my_incl[col] = s_prefix[col] + s_agg[col];
+        if (flagged) {
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();
+                st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | kFlagPrefix);
+            }
+        }
     }
 }
 
@@ -439,22 +468,74 @@ layout_finalize_kernel(FinalArgs a) {
     const int n = nt * a.K;
     const int64_t e0 = t0 * a.K;
 
+    // The routing and the weights are inputs of the layout call: they were
+    // complete before the scan kernel passed its own dependency wait, so they
+    // can be fetched before this kernel's wait (which covers the scan's outputs).
+    __shared__ int32_t s_warp[2 * (kFinalizeThreads / 32)];
+    int32_t e_r[kFinalizePerThread];
+    float w_r[kFinalizePerThread];
+#pragma unroll
+    for (int u = 0; u < kFinalizePerThread; ++u) {
+        const int i = tid + u * kFinalizeThreads;
+        e_r[u] = i < n ? a.topk_idx[e0 + i] : -1;
+        w_r[u] = (i < n && a.topk_w) ? a.topk_w[e0 + i] : 0.0f;
+    }
+    for (int i = tid; i < a.E; i += kFinalizeThreads) s_rank[i] = i / a.m;
+    for (int i = tid; i < nt * a.R; i += kFinalizeThreads) s_rs[i] = -1;
+    // the call counter only changes in this kernel (block 0, below)
+    const bool header = blockIdx.x == 0 && tid == 0;
+    const uint32_t epoch = header ? ld_relaxed_gpu(&a.ws.hdr->epoch) : 0u;
+
     pdl_wait();
     pdl_trigger();          // one wave of CTAs: the dispatch grid may become resident now
-    __shared__ int32_t s_warp[2 * (kFinalizeThreads / 32)];
-    for (int i = tid; i < a.E; i += kFinalizeThreads) s_rank[i] = i / a.m;
+    // the scan's per-entry ranks (loaded for every entry, so that they do not
+    // wait for the ids) and, inside expert_offsets, its totals
+    int32_t er_r[kFinalizePerThread], pr_r[kFinalizePerThread];
+#pragma unroll
+    for (int u = 0; u < kFinalizePerThread; ++u) {
+        const int i = tid + u * kFinalizeThreads;
+        er_r[u] = i < n ? __ldcg(a.ws.erank + e0 + i) : 0;
+        pr_r[u] = i < n ? __ldcg(a.ws.prank + e0 + i) : 0;
+    }
+    const uint32_t k1 = header ? ld_relaxed_gpu(&a.ws.hdr->k1_err) : 0u;   // the scan's error bits
     const int32_t* totals = a.ws.tile_incl + static_cast<int64_t>(a.num_tiles - 1) * vec_width(a.E);
     expert_offsets(totals, a.E, s_eoff, s_poff, s_warp);
-    for (int i = tid; i < n; i += kFinalizeThreads) {
-        int e = a.topk_idx[e0 + i];
-        if (e < 0 || e >= a.E) e = -1;
-        s_idx[i] = e;
-        s_er[i] = e >= 0 ? a.ws.erank[e0 + i] : 0;
-        s_pr[i] = e >= 0 ? a.ws.prank[e0 + i] : 0;
+#pragma unroll
+    for (int u = 0; u < kFinalizePerThread; ++u) {
+        const int i = tid + u * kFinalizeThreads;
+        if (i < n) {
+            const int e = (e_r[u] < 0 || e_r[u] >= a.E) ? -1 : e_r[u];
+            s_idx[i] = e;
+            s_er[i] = e >= 0 ? er_r[u] : 0;
+            s_pr[i] = e >= 0 ? pr_r[u] : 0;
+        }
     }
-    for (int i = tid; i < nt * a.R; i += kFinalizeThreads) s_rs[i] = -1;
     __syncthreads();
 
+    // block 0: the counts and offsets, the status word and the workspace
+    // reset, first, so that they overlap the other blocks' scatter writes
+    if (blockIdx.x == 0) {
+        for (int e = tid; e <= a.E; e += kFinalizeThreads) {
+            a.expert_offset[e] = s_eoff[e];
+            if (!a.src_order) a.recv_expert_offset[e] = s_poff[e];
+            if (e < a.E) a.tokens_per_expert[e] = s_eoff[e + 1] - s_eoff[e];
+        }
+        for (int r = tid; r <= a.R; r += kFinalizeThreads) {
+            a.rank_offset[r] = a.src_order ? r * a.T : s_poff[r * a.m];
+            if (r < a.R) a.tokens_per_rank[r] = s_poff[(r + 1) * a.m] - s_poff[r * a.m];
+        }
+        if (header) {
+            // move the scan's error bits into the status word; the next call's
+            // scan starts from a fresh ticket and generation (no waits here:
+            // both header words were loaded with the other inputs)
+            if (k1) {
+                atomicOr(a.status, k1);
+                a.ws.hdr->k1_err = 0u;
+            }
+            a.ws.hdr->ticket = 0u;
+            a.ws.hdr->epoch = (epoch + 1u) % kGenMask;
+        }
+    }
     const int64_t n_entries = static_cast<int64_t>(a.T) * a.K;
     // clamped: after a failed scan the offsets may be stale
     const int64_t n_valid = min(max(static_cast<int64_t>(s_eoff[a.E]), int64_t{0}), n_entries);
@@ -487,13 +568,16 @@ layout_finalize_kernel(FinalArgs a) {
     }
     __syncthreads();
     for (int i = tid; i < nt * a.R; i += kFinalizeThreads) a.recv_slot[t0 * a.R + i] = s_rs[i];
-    for (int i = tid; i < n; i += kFinalizeThreads) {
+#pragma unroll
+    for (int u = 0; u < kFinalizePerThread; ++u) {
+        const int i = tid + u * kFinalizeThreads;
+        if (i >= n) continue;
         const int e = s_idx[i];
         const int32_t es = s_er[i];
         if (e < 0 || es < 0) continue;
         const int tl = div_small(i, inv_k);
         a.expert_src_row[es] = s_rs[tl * a.R + s_rank[e]];
-        a.expert_weight[es] = a.topk_w ? a.topk_w[e0 + i] : 0.0f;
+        a.expert_weight[es] = w_r[u];
     }
 
     // tails past the last used rows, spread over all blocks
@@ -513,25 +597,6 @@ layout_finalize_kernel(FinalArgs a) {
     for (int64_t i = n_valid + gtid; i < n_entries; i += gstride) {
         a.expert_src_row[i] = -1;
         a.expert_weight[i] = 0.0f;
-    }
-    if (blockIdx.x == 0) {
-        for (int e = tid; e <= a.E; e += kFinalizeThreads) {
-            a.expert_offset[e] = s_eoff[e];
-            if (!a.src_order) a.recv_expert_offset[e] = s_poff[e];
-            if (e < a.E) a.tokens_per_expert[e] = s_eoff[e + 1] - s_eoff[e];
-        }
-        for (int r = tid; r <= a.R; r += kFinalizeThreads) {
-            a.rank_offset[r] = a.src_order ? r * a.T : s_poff[r * a.m];
-            if (r < a.R) a.tokens_per_rank[r] = s_poff[(r + 1) * a.m] - s_poff[r * a.m];
-        }
-        if (tid == 0) {
-            // move the scan's error bits into the status word; the next call's
-            // scan starts from a fresh ticket and generation
-            const uint32_t k1 = atomicExch(&a.ws.hdr->k1_err, 0u);
-            if (k1) atomicOr(a.status, k1);
-            a.ws.hdr->ticket = 0u;
-            a.ws.hdr->epoch = (a.ws.hdr->epoch + 1u) % kGenMask;
-        }
     }
     if (!a.src_order && s_poff[a.E] > a.capacity) bad = true;
     if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
