@@ -36,6 +36,11 @@ L2_FLUSH_BYTES = 256 << 20
 
 # ------------------------------------------------------------ byte accounting
 
+# Secondary legs run after the timed step (each reported under "ops"); the
+# headline step and its layout / dispatch split always run.
+LEGS = ("fp8", "mxfp8", "backward", "ll", "sources", "e2e")
+
+
 def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
     """Minimum HBM bytes of each operator: every input byte read once, every
     output byte written once (x is read once, not once per destination)."""
@@ -190,8 +195,6 @@ def run_ours(args, rank, world, local_rank):
     w = inp.topk_w.to(dev)
     y = inp.y.to(dev)
     recv, _ = ep.alloc_recv(L, H, False, device=dev)
-    recv8, scales8 = ep.alloc_recv(L, H, ep.MOE_FORMAT_FP8, device=dev)
-    recvmx, scalesmx = ep.alloc_recv(L, H, ep.MOE_FORMAT_MXFP8, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
@@ -258,106 +261,128 @@ def run_ours(args, rank, world, local_rank):
     dis = [e[1].elapsed_time(e[2]) for e in ev_split]
     ms_step = max_over_ranks(ms_step, world, dev)
 
-    # FP8 dispatch, timed the same way (secondary figure)
-    ev8 = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 3))]
-    for e in ev8:
-        flush()
-        e[0].record(stream)
-        ep.moe_dispatch(x, L, ep.MOE_FORMAT_FP8, recv8, scales8, stream)
-        e[1].record(stream)
-    torch.cuda.synchronize(dev)
-    dis8 = [e[0].elapsed_time(e[1]) for e in ev8]
-    evmx = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(max(args.steps // 4, 3))]
-    for e in evmx:
-        flush()
-        e[0].record(stream)
-        ep.moe_dispatch(x, L, ep.MOE_FORMAT_MXFP8, recvmx, scalesmx, stream)
-        e[1].record(stream)
-    torch.cuda.synchronize(dev)
-    dismx = [e[0].elapsed_time(e[1]) for e in evmx]
+    peak, peak_kind = measured_peaks()
+    gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
+    n_sec = max(args.steps // 4, 3)
+    legs = set(LEGS) if args.legs == "all" else set() if args.legs == "none" else set(args.legs.split(","))
 
-    # backward pair (secondary figures): gradients of the receive rows and of the output
-    grad_recv = torch.empty_like(recv).normal_()
-    grad_out = torch.empty_like(out).normal_()
-    grad_x = torch.empty_like(x)
-    grad_y = torch.empty_like(y)
-    grad_w = torch.empty_like(w)
-    evb = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(args.steps // 4, 3))]
-    for e in evb:
-        flush()
-        e[0].record(stream)
-        ep.moe_dispatch_backward(grad_recv, L, grad_x, stream)
-        e[1].record(stream)
-        ep.moe_combine_backward(grad_out, y, L, w, grad_y, grad_w, stream)
-        e[2].record(stream)
-    torch.cuda.synchronize(dev)
-    dbwd = [e[0].elapsed_time(e[1]) for e in evb]
-    cbwd = [e[1].elapsed_time(e[2]) for e in evb]
+    def timed(body, n, marks):
+        """n flushed repetitions of body(events) with `marks` events each;
+        the mean time between consecutive events in ms."""
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(n)]
+        for e in evs:
+            flush()
+            body(e)
+        torch.cuda.synchronize(dev)
+        return [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(marks - 1)]
+
+    def hbm_op(us_ms, nbytes, **extra):
+        return {"us": round(us_ms * 1e3, 2), "bytes": nbytes, "GB/s": round(gbps(nbytes, us_ms), 1),
+                "frac": round(gbps(nbytes, us_ms) / peak, 4), **extra}
+
+    com_ms = statistics.mean(com)
+    achieved = ab["combine"] / (com_ms * 1e-3) / 1e9
+    ops = {
+        "note": "layout and dispatch_bf16 from a separate pass with an event between them",
+        "layout": {"us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"]},
+        "dispatch_bf16": hbm_op(statistics.mean(dis), ab["dispatch"],
+                                tokens_per_s=round(T / (statistics.mean(dis) * 1e-3), 1)),
+        "combine": hbm_op(com_ms, ab["combine"], tokens_per_s=round(T / (com_ms * 1e-3), 1)),
+    }
+
+    # FP8 and MXFP8 dispatch on the same layout (secondary figures)
+    for fmt, key, leg in ((ep.MOE_FORMAT_FP8, "dispatch_fp8", "fp8"), (ep.MOE_FORMAT_MXFP8, "dispatch_mxfp8", "mxfp8")):
+        if leg not in legs:
+            continue
+        rq, rs = ep.alloc_recv(L, H, fmt, device=dev)
+
+        def body(e, fmt=fmt, rq=rq, rs=rs):
+            e[0].record(stream)
+            ep.moe_dispatch(x, L, fmt, rq, rs, stream)
+            e[1].record(stream)
+        ops[key] = hbm_op(timed(body, n_sec, 2)[0], ab[key])
+        del rq, rs
+
+    # backward pair: gradients of the receive rows and of the output
+    if "backward" in legs:
+        grad_recv = torch.empty_like(recv).normal_()
+        grad_out = torch.empty_like(out).normal_()
+        grad_x = torch.empty_like(x)
+        grad_y = torch.empty_like(y)
+        grad_w = torch.empty_like(w)
+
+        def body(e):
+            e[0].record(stream)
+            ep.moe_dispatch_backward(grad_recv, L, grad_x, stream)
+            e[1].record(stream)
+            ep.moe_combine_backward(grad_out, y, L, w, grad_y, grad_w, stream)
+            e[2].record(stream)
+        dbwd, cbwd = timed(body, n_sec, 3)
+        ops["dispatch_backward"] = hbm_op(dbwd, ab["dispatch_backward"])
+        ops["combine_backward"] = hbm_op(cbwd, ab["combine_backward"])
+        del grad_recv, grad_out, grad_x, grad_y, grad_w
     st, flags = ep.moe_layout_read_status(L, stream)
     if st != 0:
         raise RuntimeError(f"device status {st} after the secondary legs")
 
     # low-latency (decode) path: 128 tokens of the same shape, fixed capacity 128 per expert
-    T_ll = 128
-    x_ll, idx_ll, w_ll = x[:T_ll].contiguous(), idx[:T_ll].contiguous(), w[:T_ll].contiguous()
-    recv_ll = torch.empty(E * T_ll, H, dtype=torch.bfloat16, device=dev)
-    tpe_ll = torch.empty(E, dtype=torch.int32, device=dev)
-    slot_ll = torch.empty(T_ll, K, dtype=torch.int32, device=dev)
-    st_ll = torch.zeros(1, dtype=torch.int32, device=dev)
-    out_ll = torch.empty(T_ll, H, dtype=torch.bfloat16, device=dev)
-    evl = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(max(args.steps // 4, 3))]
-    for e in evl:
-        flush()
-        e[0].record(stream)
-        ep.moe_ll_dispatch(x_ll, idx_ll, E, T_ll, recv_ll, tpe_ll, slot_ll, st_ll, stream)
-        e[1].record(stream)
-        ep.moe_ll_combine(recv_ll, slot_ll, w_ll, E, T_ll, out_ll, st_ll, stream)
-        e[2].record(stream)
-    torch.cuda.synchronize(dev)
-    if int(st_ll.item()) != 0:
-        raise RuntimeError("low-latency path reported a device error")
-    lld = [e[0].elapsed_time(e[1]) for e in evl]
-    llc = [e[1].elapsed_time(e[2]) for e in evl]
-    ll_bytes = 2 * T_ll * H + 2 * H * T_ll * K + 4 * T_ll * K    # rows read, one row per entry written
-    del recv_ll, grad_recv, grad_y, recv8, scales8, recvmx, scalesmx
+    if "ll" in legs:
+        T_ll = 128
+        x_ll, idx_ll, w_ll = x[:T_ll].contiguous(), idx[:T_ll].contiguous(), w[:T_ll].contiguous()
+        recv_ll = torch.empty(E * T_ll, H, dtype=torch.bfloat16, device=dev)
+        tpe_ll = torch.empty(E, dtype=torch.int32, device=dev)
+        slot_ll = torch.empty(T_ll, K, dtype=torch.int32, device=dev)
+        st_ll = torch.zeros(1, dtype=torch.int32, device=dev)
+        out_ll = torch.empty(T_ll, H, dtype=torch.bfloat16, device=dev)
+
+        def body(e):
+            e[0].record(stream)
+            ep.moe_ll_dispatch(x_ll, idx_ll, E, T_ll, recv_ll, tpe_ll, slot_ll, st_ll, stream)
+            e[1].record(stream)
+            ep.moe_ll_combine(recv_ll, slot_ll, w_ll, E, T_ll, out_ll, st_ll, stream)
+            e[2].record(stream)
+        lld, llc = timed(body, n_sec, 3)
+        if int(st_ll.item()) != 0:
+            raise RuntimeError("low-latency path reported a device error")
+        ll_bytes = 2 * T_ll * H + 2 * H * T_ll * K + 4 * T_ll * K    # rows read, one row per entry written
+        ops["ll_dispatch_T128"] = {"us": round(lld * 1e3, 2), "bytes": ll_bytes, "GB/s": round(gbps(ll_bytes, lld), 1)}
+        ops["ll_combine_T128"] = {"us": round(llc * 1e3, 2), "bytes": ll_bytes, "GB/s": round(gbps(ll_bytes, llc), 1)}
+        del recv_ll
 
     # multi-source receive: all eight ranks' tokens of this shape at once (S = 8
     # sources of T tokens, one region of 8T rows per destination rank)
-    S_ms = 8
-    inp_ms = make_inputs(wl.scaled(S_ms * T), seed=1000 + rank, with_y=False)
-    L_ms = ep.Layout(S_ms * T, K, E, R, device=dev, sources=S_ms)
-    x_ms, idx_ms, w_ms = inp_ms.x.to(dev), inp_ms.topk_idx.to(dev), inp_ms.topk_w.to(dev)
-    gen = torch.Generator(device=dev).manual_seed(77 + rank)
-    y_ms = torch.randn(S_ms * T * K, H, device=dev, generator=gen).to(torch.bfloat16)
-    recv_ms, _ = ep.alloc_recv(L_ms, H, False, device=dev)
-    out_ms = torch.empty(S_ms * T, H, dtype=torch.bfloat16, device=dev)
-    evm = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(max(args.steps // 10, 3))]
-    for e in evm:
-        flush()
-        e[0].record(stream)
-        ep.moe_dispatch_layout(idx_ms, w_ms, E, R, L_ms, stream)
-        e[1].record(stream)
-        ep.moe_dispatch(x_ms, L_ms, False, recv_ms, None, stream)
-        e[2].record(stream)
-        ep.moe_combine(y_ms, L_ms, w_ms, out_ms, stream)
-        e[3].record(stream)
-    torch.cuda.synchronize(dev)
-    st, flags = ep.moe_layout_read_status(L_ms, stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st} in the multi-source leg")
-    msl = statistics.mean(e[0].elapsed_time(e[1]) for e in evm)
-    msd = statistics.mean(e[1].elapsed_time(e[2]) for e in evm)
-    msc = statistics.mean(e[2].elapsed_time(e[3]) for e in evm)
-    ab_ms = algorithmic_bytes(S_ms * T, H, E, R, K, int(L_ms.tokens_per_rank.sum().item()),
-                              int(L_ms.expert_offset[E].item()), L_ms.capacity)
-    del x_ms, y_ms, recv_ms, out_ms, L_ms
+    if "sources" in legs:
+        S_ms = 8
+        inp_ms = make_inputs(wl.scaled(S_ms * T), seed=1000 + rank, with_y=False)
+        L_ms = ep.Layout(S_ms * T, K, E, R, device=dev, sources=S_ms)
+        x_ms, idx_ms, w_ms = inp_ms.x.to(dev), inp_ms.topk_idx.to(dev), inp_ms.topk_w.to(dev)
+        gen = torch.Generator(device=dev).manual_seed(77 + rank)
+        y_ms = torch.randn(S_ms * T * K, H, device=dev, generator=gen).to(torch.bfloat16)
+        recv_ms, _ = ep.alloc_recv(L_ms, H, False, device=dev)
+        out_ms = torch.empty(S_ms * T, H, dtype=torch.bfloat16, device=dev)
 
-    e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if rank == 0 else None
+        def body(e):
+            e[0].record(stream)
+            ep.moe_dispatch_layout(idx_ms, w_ms, E, R, L_ms, stream)
+            e[1].record(stream)
+            ep.moe_dispatch(x_ms, L_ms, False, recv_ms, None, stream)
+            e[2].record(stream)
+            ep.moe_combine(y_ms, L_ms, w_ms, out_ms, stream)
+            e[3].record(stream)
+        msl, msd, msc = timed(body, max(args.steps // 10, 3), 4)
+        st, flags = ep.moe_layout_read_status(L_ms, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} in the multi-source leg")
+        ab_ms = algorithmic_bytes(S_ms * T, H, E, R, K, int(L_ms.tokens_per_rank.sum().item()),
+                                  int(L_ms.expert_offset[E].item()), L_ms.capacity)
+        ops["multi_source_S8"] = {"note": f"8 sources x {T} tokens, one region of {8 * T} rows per destination rank",
+                                  "layout_us": round(msl * 1e3, 2),
+                                  "dispatch_bf16": hbm_op(msd, ab_ms["dispatch"]),
+                                  "combine": hbm_op(msc, ab_ms["combine"])}
+        del x_ms, y_ms, recv_ms, out_ms, L_ms
 
-    peak, peak_kind = measured_peaks()
-    com_ms = statistics.mean(com)
-    achieved = ab["combine"] / (com_ms * 1e-3) / 1e9
-    gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
+    e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if (rank == 0 and "e2e" in legs) else None
+
     result = {
         "metric": METRIC,
         "value": round(aggregate_gbps(step_bytes, ms_step, world), 1),
@@ -376,41 +401,7 @@ def run_ours(args, rank, world, local_rank):
                    "step": "layout + bf16 dispatch + combine", "l2": "flushed between steps (256 MB write, then 256 MB read of another buffer)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
-        "ops": {
-            "note": "layout and dispatch_bf16 from a separate pass with an event between them",
-            "layout": {"us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"]},
-            "dispatch_bf16": {"us": round(statistics.mean(dis) * 1e3, 2), "bytes": ab["dispatch"],
-                              "GB/s": round(gbps(ab["dispatch"], statistics.mean(dis)), 1),
-                              "frac": round(gbps(ab["dispatch"], statistics.mean(dis)) / peak, 4),
-                              "tokens_per_s": round(T / (statistics.mean(dis) * 1e-3), 1)},
-            "combine": {"us": round(com_ms * 1e3, 2), "bytes": ab["combine"], "GB/s": round(achieved, 1),
-                        "frac": round(achieved / peak, 4), "tokens_per_s": round(T / (com_ms * 1e-3), 1)},
-            "dispatch_fp8": {"us": round(statistics.mean(dis8) * 1e3, 2), "bytes": ab["dispatch_fp8"],
-                             "GB/s": round(gbps(ab["dispatch_fp8"], statistics.mean(dis8)), 1),
-                             "frac": round(gbps(ab["dispatch_fp8"], statistics.mean(dis8)) / peak, 4)},
-            "dispatch_mxfp8": {"us": round(statistics.mean(dismx) * 1e3, 2), "bytes": ab["dispatch_mxfp8"],
-                               "GB/s": round(gbps(ab["dispatch_mxfp8"], statistics.mean(dismx)), 1),
-                               "frac": round(gbps(ab["dispatch_mxfp8"], statistics.mean(dismx)) / peak, 4)},
-            "dispatch_backward": {"us": round(statistics.mean(dbwd) * 1e3, 2), "bytes": ab["dispatch_backward"],
-                                  "GB/s": round(gbps(ab["dispatch_backward"], statistics.mean(dbwd)), 1),
-                                  "frac": round(gbps(ab["dispatch_backward"], statistics.mean(dbwd)) / peak, 4)},
-            "ll_dispatch_T128": {"us": round(statistics.mean(lld) * 1e3, 2), "bytes": ll_bytes,
-                                 "GB/s": round(gbps(ll_bytes, statistics.mean(lld)), 1)},
-            "ll_combine_T128": {"us": round(statistics.mean(llc) * 1e3, 2), "bytes": ll_bytes,
-                                "GB/s": round(gbps(ll_bytes, statistics.mean(llc)), 1)},
-            "combine_backward": {"us": round(statistics.mean(cbwd) * 1e3, 2), "bytes": ab["combine_backward"],
-                                 "GB/s": round(gbps(ab["combine_backward"], statistics.mean(cbwd)), 1),
-                                 "frac": round(gbps(ab["combine_backward"], statistics.mean(cbwd)) / peak, 4)},
-            "multi_source_S8": {
-                "note": f"8 sources x {T} tokens, one region of {8 * T} rows per destination rank",
-                "layout_us": round(msl * 1e3, 2),
-                "dispatch_bf16": {"us": round(msd * 1e3, 2), "bytes": ab_ms["dispatch"],
-                                  "GB/s": round(gbps(ab_ms["dispatch"], msd), 1),
-                                  "frac": round(gbps(ab_ms["dispatch"], msd) / peak, 4)},
-                "combine": {"us": round(msc * 1e3, 2), "bytes": ab_ms["combine"],
-                            "GB/s": round(gbps(ab_ms["combine"], msc), 1),
-                            "frac": round(gbps(ab_ms["combine"], msc) / peak, 4)}},
-        },
+        "ops": ops,
         "roofline": {"bound": "hbm", "kernel": "combine_kernel<8>", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
@@ -572,7 +563,11 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--legs", default="all",
+                    help="secondary legs after the timed step: 'all', 'none' or a comma list of " + ",".join(LEGS))
     args = ap.parse_args()
+    if args.legs not in ("all", "none") and not set(args.legs.split(",")) <= set(LEGS):
+        ap.error(f"--legs: choose 'all', 'none' or from {','.join(LEGS)}")
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
 

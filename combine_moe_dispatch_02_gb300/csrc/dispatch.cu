@@ -552,25 +552,29 @@ dispatch_lsu_kernel(DispatchArgs a) {
                 const MxQuant mq = quantize_group_share_mx(v[u][0], v[u][1]);
                 q0 = mq.q0; q1 = mq.q1; word = mq.scales;
             }
+            // this lane's two column offsets (the same for every destination row)
+            const int c0 = lsu_col<FMT>(col0[u], lane, 0), c1 = lsu_col<FMT>(col0[u], lane, 1);
+            const bool in0 = c0 < a.H, in1 = c1 < a.H;
+            const bool scale_lane = FMT != 0 && in0 && (lane & 7) == 0;
             for (int rbase = 0; rbase < a.R; rbase += 32) {
                 const int32_t my_slot = rbase == 0 ? slot_lane[u]
                                                    : (lane + rbase < a.R ? __ldg(a.recv_slot + t * a.R + rbase + lane) : -1);
-                const int nr = min(32, a.R - rbase);
-                for (int r = 0; r < nr; ++r) {
-                    const int32_t slot = __shfl_sync(0xffffffffu, my_slot, r);
-                    if (slot < 0) continue;
-                    if (slot >= a.capacity) { bad = true; continue; }
-#pragma unroll
-                    for (int j = 0; j < 2; ++j) {
-                        const int col = lsu_col<FMT>(col0[u], lane, j);
-                        if (col >= a.H) continue;
-                        if constexpr (FMT != 0) {
-                            *reinterpret_cast<uint2*>(a.recv + static_cast<int64_t>(slot) * a.H + col) = j ? q1 : q0;
-                            if (j == 0 && (lane & 7) == 0)
-                                a.recv_scales[static_cast<int64_t>(slot) * nb_row + col / 128] = word;
-                        } else {
-                            *reinterpret_cast<uint4*>(a.recv + (static_cast<int64_t>(slot) * a.H + col) * 2) = v[u][j];
-                        }
+                if (my_slot >= a.capacity) bad = true;          // flagged, never written
+                // walk only the ranks this token goes to
+                uint32_t dests = __ballot_sync(0xffffffffu, my_slot >= 0 && my_slot < a.capacity);
+                while (dests) {
+                    const int r = __ffs(dests) - 1;
+                    dests &= dests - 1;
+                    const int64_t slot = __shfl_sync(0xffffffffu, my_slot, r);
+                    if constexpr (FMT != 0) {
+                        uint8_t* row = a.recv + slot * a.H;
+                        if (in0) *reinterpret_cast<uint2*>(row + c0) = q0;
+                        if (in1) *reinterpret_cast<uint2*>(row + c1) = q1;
+                        if (scale_lane) a.recv_scales[slot * nb_row + (c0 >> 7)] = word;
+                    } else {
+                        uint8_t* row = a.recv + slot * a.H * 2;
+                        if (in0) *reinterpret_cast<uint4*>(row + c0 * 2) = v[u][0];
+                        if (in1) *reinterpret_cast<uint4*>(row + c1 * 2) = v[u][1];
                     }
                 }
             }
