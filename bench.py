@@ -38,7 +38,9 @@ L2_FLUSH_BYTES = 256 << 20
 
 # Secondary legs run after the timed step (each reported under "ops"); the
 # headline step and its layout / dispatch split always run.
-LEGS = ("fp8", "mxfp8", "backward", "ll", "sources", "e2e")
+LEGS = ("fp8", "mxfp8", "backward", "ll", "sources", "channels", "e2e")
+# CTA counts of the channel sweep (the pages fill NVLink with 4 SMs; HBM needs many more)
+SWEEP_CTAS = (4, 8, 16, 32, 64, 152, 304, 608, 1216)
 
 
 def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
@@ -380,6 +382,26 @@ def run_ours(args, rank, world, local_rank):
                                   "dispatch_bf16": hbm_op(msd, ab_ms["dispatch"]),
                                   "combine": hbm_op(msc, ab_ms["combine"])}
         del x_ms, y_ms, recv_ms, out_ms, L_ms
+
+    # how many CTAs ("channels") the HBM-bound operators need: bf16 dispatch (one
+    # warp per CTA) and combine (256 threads per CTA) at fixed CTA counts
+    if "channels" in legs:
+        sweep = {"note": "GB/s at a fixed number of CTAs; default = the operator's own grid", "dispatch_bf16": {},
+                 "combine": {}}
+        for n_cta in SWEEP_CTAS + (0,):
+            def body_d(e, n_cta=n_cta):
+                e[0].record(stream)
+                ep.moe_dispatch(x, L, False, recv, None, stream, num_channels=n_cta, variant=1)
+                e[1].record(stream)
+
+            def body_c(e, n_cta=n_cta):
+                e[0].record(stream)
+                ep.moe_combine(y, L, w, out, stream, num_channels=n_cta)
+                e[1].record(stream)
+            key = str(n_cta) if n_cta else "default"
+            sweep["dispatch_bf16"][key] = round(gbps(ab["dispatch"], timed(body_d, 10, 2)[0]), 1)
+            sweep["combine"][key] = round(gbps(ab["combine"], timed(body_c, 10, 2)[0]), 1)
+        ops["channel_sweep"] = sweep
 
     e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if (rank == 0 and "e2e" in legs) else None
 

@@ -481,11 +481,12 @@ dispatch_fp8_ws_kernel(DispatchArgs a) {
 // 16-byte vector path ------------------------------------------------------
 
 // No shared-memory staging: a warp moves one 512-column segment of one token
-// per item.  Each lane loads two 16-byte vectors, so every load and store
-// instruction of the warp covers whole 32-byte sectors.  bf16: lane l takes
-// columns l*8 and 256 + l*8 of the segment.  FP8: the eight lanes 8g..8g+7
-// hold block g of the segment (lane li: columns li*8 and 64 + li*8 of it) and
-// reduce its amax with shuffles.  U items (2 or 4) are in flight per warp (all
+// per item.  Each lane loads two 16-byte vectors.  bf16: lane l takes columns
+// l*8 and 256 + l*8 of the segment.  FP8 / MXFP8: the eight lanes 8g..8g+7
+// hold 128-column block g of the segment, lane li its columns li*16 ..
+// li*16+15, and reduce the block amax with shuffles; each lane then writes its
+// 16 codes with one 16-byte store per destination row (eight lanes fill a
+// whole 128-byte line).  U items (2 or 4) are in flight per warp (all
 // their loads are issued before any store).  The destination rows come from
 // recv_slot: lane r holds the slot of rank r and the warp walks the ranks with
 // shuffles.
@@ -501,12 +502,90 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 
 template <int FMT>
 __device__ __forceinline__ int lsu_col(int col0, int lane, int j) {
-    if constexpr (FMT != 0) return col0 + (lane >> 3) * 128 + j * 64 + (lane & 7) * 8;
+    if constexpr (FMT != 0) return col0 + (lane >> 3) * 128 + (lane & 7) * 16 + j * 8;
     return col0 + j * 256 + lane * 8;
 }
 
+// One batch: U items of a warp (item = one 512-column segment of one token),
+// their source vectors and the lane's recv_slot entry.
+template <int U>
+struct LsuBatch {
+    uint4 v[U][2];
+    int32_t slot_lane[U];
+    int64_t tok[U];
+    int col0[U];
+    bool live[U];
+};
+
+template <int FMT, int U>
+__device__ __forceinline__ void lsu_load(LsuBatch<U>& b, const DispatchArgs& a, int64_t item0, int64_t n_warps,
+                                         int64_t n_items, int nseg, int lane) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int64_t item = item0 + u * n_warps;
+        b.live[u] = item < n_items;                      // warp-uniform
+        const int64_t t = b.live[u] ? item / nseg : 0;
+        const int g = b.live[u] ? static_cast<int>(item - t * nseg) : 0;
+        b.tok[u] = t;
+        b.col0[u] = g * kSegElems;
+        b.slot_lane[u] = (b.live[u] && lane < a.R) ? __ldg(a.recv_slot + t * a.R + lane) : -1;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int col = lsu_col<FMT>(b.col0[u], lane, j);
+            b.v[u][j] = (b.live[u] && col < a.H) ? ld_nc_v4(a.x + (t * a.H + col) * 2) : make_uint4(0u, 0u, 0u, 0u);
+        }
+    }
+}
+
+template <int FMT, int U>
+__device__ __forceinline__ void lsu_store(const LsuBatch<U>& b, const DispatchArgs& a, int nb_row, int lane,
+                                          bool& bad) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        if (!b.live[u]) continue;
+        const int64_t t = b.tok[u];
+        uint2 q0 = make_uint2(0u, 0u), q1 = q0;
+        uint32_t word = 0;
+        if constexpr (FMT == 1) {
+            const BlockQuant bq = quantize_block_share(b.v[u][0], b.v[u][1]);
+            q0 = bq.q0; q1 = bq.q1; word = __float_as_uint(bq.scale);
+        } else if constexpr (FMT == 2) {
+            const MxQuant mq = quantize_group_share_mx16(b.v[u][0], b.v[u][1]);
+            q0 = mq.q0; q1 = mq.q1; word = mq.scales;
+        }
+        const uint4 q = make_uint4(q0.x, q0.y, q1.x, q1.y);     // the lane's 16 consecutive codes
+        // this lane's two column offsets (the same for every destination row)
+        const int c0 = lsu_col<FMT>(b.col0[u], lane, 0), c1 = lsu_col<FMT>(b.col0[u], lane, 1);
+        const bool in0 = c0 < a.H, in1 = c1 < a.H;
+        const bool scale_lane = FMT != 0 && in0 && (lane & 7) == 0;
+        for (int rbase = 0; rbase < a.R; rbase += 32) {
+            const int32_t my_slot = rbase == 0 ? b.slot_lane[u]
+                                               : (lane + rbase < a.R ? __ldg(a.recv_slot + t * a.R + rbase + lane) : -1);
+            if (my_slot >= a.capacity) bad = true;          // flagged, never written
+            // walk only the ranks this token goes to
+            uint32_t dests = __ballot_sync(0xffffffffu, my_slot >= 0 && my_slot < a.capacity);
+            while (dests) {
+                const int r = __ffs(dests) - 1;
+                dests &= dests - 1;
+                const int64_t slot = __shfl_sync(0xffffffffu, my_slot, r);
+                if constexpr (FMT != 0) {
+                    uint8_t* row = a.recv + slot * a.H;
+                    if (in0) *reinterpret_cast<uint4*>(row + c0) = q;     // c1 = c0 + 8: one 16-byte store
+                    if (scale_lane) a.recv_scales[slot * nb_row + (c0 >> 7)] = word;
+                } else {
+                    uint8_t* row = a.recv + slot * a.H * 2;
+                    if (in0) *reinterpret_cast<uint4*>(row + c0 * 2) = b.v[u][0];
+                    if (in1) *reinterpret_cast<uint4*>(row + c1 * 2) = b.v[u][1];
+                }
+            }
+        }
+    }
+}
+
 // FMT 0: bf16 rows; 1: FP8 with fp32 1x128 scales; 2: MXFP8 (E8M0 1x32 scales).
-// U items in flight per warp.
+// Software-pipelined in batches of U items per warp: the next batch's loads
+// are issued before the current batch is quantised and stored, so the load
+// latency overlaps the arithmetic and the stores (2U items in flight).
 template <int FMT, int U>
 __global__ void __launch_bounds__(kLsuThreads)
 dispatch_lsu_kernel(DispatchArgs a) {
@@ -517,68 +596,20 @@ dispatch_lsu_kernel(DispatchArgs a) {
     const int nseg = (a.H + kSegElems - 1) / kSegElems;
     const int64_t n_items = static_cast<int64_t>(a.T) * nseg;
     const int nb_row = a.H / 128;
+    const int64_t stride = U * n_warps;
     bool bad = false;
-    for (int64_t item0 = warp_id; item0 < n_items; item0 += U * n_warps) {
-        uint4 v[U][2];
-        int32_t slot_lane[U];
-        int64_t tok[U];
-        int col0[U];
-        bool live[U];
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int64_t item = item0 + u * n_warps;
-            live[u] = item < n_items;                      // warp-uniform
-            const int64_t t = live[u] ? item / nseg : 0;
-            const int g = live[u] ? static_cast<int>(item - t * nseg) : 0;
-            tok[u] = t;
-            col0[u] = g * kSegElems;
-            slot_lane[u] = (live[u] && lane < a.R) ? __ldg(a.recv_slot + t * a.R + lane) : -1;
-#pragma unroll
-            for (int j = 0; j < 2; ++j) {
-                const int col = lsu_col<FMT>(col0[u], lane, j);
-                v[u][j] = (live[u] && col < a.H) ? ld_nc_v4(a.x + (t * a.H + col) * 2) : make_uint4(0u, 0u, 0u, 0u);
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < U; ++u) {
-            if (!live[u]) continue;
-            const int64_t t = tok[u];
-            uint2 q0 = make_uint2(0u, 0u), q1 = q0;
-            uint32_t word = 0;
-            if constexpr (FMT == 1) {
-                const BlockQuant bq = quantize_block_share(v[u][0], v[u][1]);
-                q0 = bq.q0; q1 = bq.q1; word = __float_as_uint(bq.scale);
-            } else if constexpr (FMT == 2) {
-                const MxQuant mq = quantize_group_share_mx(v[u][0], v[u][1]);
-                q0 = mq.q0; q1 = mq.q1; word = mq.scales;
-            }
-            // this lane's two column offsets (the same for every destination row)
-            const int c0 = lsu_col<FMT>(col0[u], lane, 0), c1 = lsu_col<FMT>(col0[u], lane, 1);
-            const bool in0 = c0 < a.H, in1 = c1 < a.H;
-            const bool scale_lane = FMT != 0 && in0 && (lane & 7) == 0;
-            for (int rbase = 0; rbase < a.R; rbase += 32) {
-                const int32_t my_slot = rbase == 0 ? slot_lane[u]
-                                                   : (lane + rbase < a.R ? __ldg(a.recv_slot + t * a.R + rbase + lane) : -1);
-                if (my_slot >= a.capacity) bad = true;          // flagged, never written
-                // walk only the ranks this token goes to
-                uint32_t dests = __ballot_sync(0xffffffffu, my_slot >= 0 && my_slot < a.capacity);
-                while (dests) {
-                    const int r = __ffs(dests) - 1;
-                    dests &= dests - 1;
-                    const int64_t slot = __shfl_sync(0xffffffffu, my_slot, r);
-                    if constexpr (FMT != 0) {
-                        uint8_t* row = a.recv + slot * a.H;
-                        if (in0) *reinterpret_cast<uint2*>(row + c0) = q0;
-                        if (in1) *reinterpret_cast<uint2*>(row + c1) = q1;
-                        if (scale_lane) a.recv_scales[slot * nb_row + (c0 >> 7)] = word;
-                    } else {
-                        uint8_t* row = a.recv + slot * a.H * 2;
-                        if (in0) *reinterpret_cast<uint4*>(row + c0 * 2) = v[u][0];
-                        if (in1) *reinterpret_cast<uint4*>(row + c1 * 2) = v[u][1];
-                    }
-                }
-            }
-        }
+    LsuBatch<U> cur, nxt;
+    int64_t item0 = warp_id;
+    lsu_load<FMT, U>(cur, a, item0, n_warps, n_items, nseg, lane);
+    while (item0 < n_items) {
+        // two batches per trip, so that the buffers swap roles without copies
+        lsu_load<FMT, U>(nxt, a, item0 + stride, n_warps, n_items, nseg, lane);
+        lsu_store<FMT, U>(cur, a, nb_row, lane, bad);
+        item0 += stride;
+        if (item0 >= n_items) break;
+        lsu_load<FMT, U>(cur, a, item0 + stride, n_warps, n_items, nseg, lane);
+        lsu_store<FMT, U>(nxt, a, nb_row, lane, bad);
+        item0 += stride;
     }
     pdl_trigger();
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
@@ -631,15 +662,19 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
         smem += static_cast<size_t>(S) * a.chunk_elems * 2;
     }
     if (variant == 2 || (fp8 && variant == 0)) {
-        // 16-byte vector path (the FP8 / MXFP8 default): persistent grid, occupancy-limited
-        // items in flight per warp: 4 when asked for 4+ stages, else 2
-        const int U = stages >= 4 ? 4 : 2;
+        // 16-byte vector path (the FP8 / MXFP8 default): persistent grid, occupancy-limited.
+        // Items in flight per warp = 2U (two pipelined batches of U): stages 2 -> U = 1,
+        // 4 -> U = 2, 8 -> U = 4; the default is U = 1.
+        const int U = stages >= 8 ? 4 : stages >= 4 ? 2 : 1;
         const void* fn = U == 4 ? (format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2, 4>)
                                    : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1, 4>)
                                          : reinterpret_cast<const void*>(dispatch_lsu_kernel<0, 4>))
-                                : (format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2, 2>)
+                       : U == 2 ? (format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2, 2>)
                                    : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1, 2>)
-                                         : reinterpret_cast<const void*>(dispatch_lsu_kernel<0, 2>));
+                                         : reinterpret_cast<const void*>(dispatch_lsu_kernel<0, 2>))
+                                : (format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<2, 1>)
+                                   : fp8 ? reinterpret_cast<const void*>(dispatch_lsu_kernel<1, 1>)
+                                         : reinterpret_cast<const void*>(dispatch_lsu_kernel<0, 1>));
         int per_sm = 0;
         cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kLsuThreads, 0);
         if (e != cudaSuccess) return e;
@@ -656,9 +691,14 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
             if (fp8) return launch_pdl(dispatch_lsu_kernel<1, 4>, g, b, 0, stream, a);
             return launch_pdl(dispatch_lsu_kernel<0, 4>, g, b, 0, stream, a);
         }
-        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2, 2>, g, b, 0, stream, a);
-        if (fp8) return launch_pdl(dispatch_lsu_kernel<1, 2>, g, b, 0, stream, a);
-        return launch_pdl(dispatch_lsu_kernel<0, 2>, g, b, 0, stream, a);
+        if (U == 2) {
+            if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2, 2>, g, b, 0, stream, a);
+            if (fp8) return launch_pdl(dispatch_lsu_kernel<1, 2>, g, b, 0, stream, a);
+            return launch_pdl(dispatch_lsu_kernel<0, 2>, g, b, 0, stream, a);
+        }
+        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_lsu_kernel<2, 1>, g, b, 0, stream, a);
+        if (fp8) return launch_pdl(dispatch_lsu_kernel<1, 1>, g, b, 0, stream, a);
+        return launch_pdl(dispatch_lsu_kernel<0, 1>, g, b, 0, stream, a);
     }
     if (fp8 && variant == 3) {
         const int nbc = a.chunk_elems / 128;
