@@ -9,10 +9,12 @@
 // One launch, no workspace: decode batches are small (T * K <= 4096 entries
 // here), so every CTA loads the whole routing into shared memory and computes
 // all the positions itself (warp-aggregated ranks with per-warp histograms, as
-// in the layout scan, then a scan across warps); then it copies its share of
-// the token rows with 16-byte vector loads and stores.  CTA 0 also writes the
-// slot map and the per-expert counts.  The combine for this layout is the
-// regular weighted gather over the slot map (combine.cu).
+// in the layout scan, then a scan across warps).  A CTA owns a range of
+// tokens: it reads each token row once (16-byte vectors in registers; the
+// first row's loads are issued before the ranking, so their latency hides
+// behind it) and writes it to every destination row of the token.  CTA 0 also
+// writes the slot map and the per-expert counts.  The combine for this layout
+// is the regular weighted gather over the slot map (combine.cu).
 #include "moe_common.cuh"
 
 namespace moe {
@@ -21,6 +23,7 @@ namespace {
 
 constexpr int kLLThreads = 256;
 constexpr int kLLWarps = kLLThreads / 32;
+constexpr int kLLVecs = 4;                    // 16-byte vectors per thread per column group (8192 columns)
 
 struct LLArgs {
     const uint4* x;              // [T, H/8]
@@ -32,6 +35,16 @@ struct LLArgs {
     uint32_t* status;
 };
 
+// Column group [c0, c0 + kLLVecs * kLLThreads) of token t's row (16-byte
+// vectors; t < 0 or columns past the row give zeros).
+__device__ __forceinline__ void load_group(const LLArgs& a, int t, int c0, int tid, uint4 (&v)[kLLVecs]) {
+#pragma unroll
+    for (int j = 0; j < kLLVecs; ++j) {
+        const int c = c0 + j * kLLThreads + tid;
+        v[j] = (t >= 0 && c < a.H8) ? ld_stream_v4(a.x + static_cast<int64_t>(t) * a.H8 + c) : make_uint4(0u, 0u, 0u, 0u);
+    }
+}
+
 __global__ void __launch_bounds__(kLLThreads)
 ll_dispatch_kernel(LLArgs a) {
     extern __shared__ int32_t sm[];
@@ -41,6 +54,11 @@ ll_dispatch_kernel(LLArgs a) {
     int32_t* s_hist = s_pos + n;                // [warps][E]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     pdl_wait();
+    // this CTA's tokens; the first row's first column group is loaded now
+    const int t_begin = static_cast<int>(static_cast<int64_t>(a.T) * blockIdx.x / gridDim.x);
+    const int t_end = static_cast<int>(static_cast<int64_t>(a.T) * (blockIdx.x + 1) / gridDim.x);
+    uint4 v[kLLVecs];
+    load_group(a, t_begin < t_end ? t_begin : -1, 0, tid, v);
 
     bool bad_id = false;
     for (int i = tid; i < n; i += kLLThreads) {
@@ -100,30 +118,22 @@ ll_dispatch_kernel(LLArgs a) {
     if (blockIdx.x == 0 && tid == 0) *a.status = static_cast<uint32_t>(flags | flags2);
     pdl_trigger();
 
-    // copy this CTA's entries: flat (entry, 16-byte group) loop, four in flight
-    const int64_t i0 = static_cast<int64_t>(n) * blockIdx.x / gridDim.x;
-    const int64_t i1 = static_cast<int64_t>(n) * (blockIdx.x + 1) / gridDim.x;
-    const int64_t total = (i1 - i0) * a.H8;
-    for (int64_t f = tid; f < total; f += 4 * kLLThreads) {
-        uint4 v[4];
-        int64_t dst[4];
+    // each token row once into registers, then out to the token's destination rows
+    const int group = kLLVecs * kLLThreads;                   // 16-byte vectors per column group
+    for (int t = t_begin; t < t_end; ++t) {
+        for (int c0 = 0; c0 < a.H8; c0 += group) {
+            if (t != t_begin || c0 != 0) load_group(a, t, c0, tid, v);
+            for (int k = 0; k < a.K; ++k) {
+                const int32_t row = s_pos[t * a.K + k];          // the same for every thread
+                if (row < 0) continue;
+                uint4* dst = a.recv + static_cast<int64_t>(row) * a.H8;
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int64_t g = f + u * kLLThreads;
-            dst[u] = -1;
-            if (g < total) {
-                const int64_t i = i0 + g / a.H8;
-                const int64_t c = g - (g / a.H8) * a.H8;
-                const int32_t row = s_pos[i];
-                if (row >= 0) {
-                    v[u] = ld_stream_v4(a.x + (i / a.K) * a.H8 + c);
-                    dst[u] = static_cast<int64_t>(row) * a.H8 + c;
+                for (int j = 0; j < kLLVecs; ++j) {
+                    const int c = c0 + j * kLLThreads + tid;
+                    if (c < a.H8) dst[c] = v[j];
                 }
             }
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-            if (dst[u] >= 0) a.recv[dst[u]] = v[u];
     }
 }
 
@@ -147,10 +157,11 @@ cudaError_t launch_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32
     cudaError_t err = cudaFuncSetAttribute(ll_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                            static_cast<int>(smem));
     if (err != cudaSuccess) return err;
-    // about four entries per CTA, at most two CTAs per SM
-    int64_t grid = num_channels > 0 ? num_channels : (n + 3) / 4;
+    // one token per CTA, at most two CTAs per SM (then several tokens per CTA)
+    int64_t grid = num_channels > 0 ? num_channels : T;
     const int64_t max_grid = static_cast<int64_t>(sm_count()) * 2;
     if (num_channels <= 0 && grid > max_grid) grid = max_grid;
+    if (grid > T) grid = T;
     if (grid < 1) grid = 1;
     return launch_pdl(ll_dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLLThreads), smem, stream, a);
 }

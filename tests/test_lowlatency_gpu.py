@@ -57,6 +57,7 @@ def test_ll_parity_decode_batches(T):
     (300, 64, 1024, 8, 32, 0.0, False, 2, 0),
     (256, 8, 4, 16, 1024, 0.1, True, 3, 7),     # few experts, many entries each
     (0, 64, 8, 2, 4, 0.0, False, 4, 0),
+    (40, 9224, 16, 4, 16, 0.1, False, 5, 300),    # rows wider than one column group; more channels than tokens
 ])
 def test_ll_edge_cases(T, H, E, K, cap, mask, dups, seed, channels):
     idx = random_routing(T, K, E, seed, mask_frac=mask, allow_duplicates=dups) if T else torch.zeros(0, K, dtype=torch.int32)
