@@ -296,6 +296,11 @@ def run_ours(args, rank, world, local_rank):
         torch.cuda.synchronize(dev)
         return [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(marks - 1)]
 
+    def pct(ms_list):
+        """p10 / p50 / p90 of per-repetition times, in us."""
+        q = statistics.quantiles(ms_list, n=10, method="inclusive") if len(ms_list) > 1 else [ms_list[0]] * 9
+        return {"p10": round(q[0] * 1e3, 2), "p50": round(statistics.median(ms_list) * 1e3, 2), "p90": round(q[8] * 1e3, 2)}
+
     def hbm_op(us_ms, nbytes, **extra):
         return {"us": round(us_ms * 1e3, 2), "bytes": nbytes, "GB/s": round(gbps(nbytes, us_ms), 1),
                 "frac": round(gbps(nbytes, us_ms) / peak, 4), **extra}
@@ -304,10 +309,11 @@ def run_ours(args, rank, world, local_rank):
     achieved = ab["combine"] / (com_ms * 1e-3) / 1e9
     ops = {
         "note": "per-operator times from an eager pass of the step with events between the operators",
-        "layout": {"us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"]},
+        "step_us": pct(tot),
+        "layout": {"us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"], "us_pct": pct(lay)},
         "dispatch_bf16": hbm_op(statistics.mean(dis), ab["dispatch"],
-                                tokens_per_s=round(T / (statistics.mean(dis) * 1e-3), 1)),
-        "combine": hbm_op(com_ms, ab["combine"], tokens_per_s=round(T / (com_ms * 1e-3), 1)),
+                                tokens_per_s=round(T / (statistics.mean(dis) * 1e-3), 1), us_pct=pct(dis)),
+        "combine": hbm_op(com_ms, ab["combine"], tokens_per_s=round(T / (com_ms * 1e-3), 1), us_pct=pct(com)),
     }
 
     # FP8 and MXFP8 dispatch on the same layout (secondary figures)
