@@ -638,21 +638,26 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     a.nchunk = (hidden + max_elems - 1) / max_elems;
     a.chunk_elems = ((hidden + a.nchunk - 1) / a.nchunk + gran - 1) / gran * gran;
     a.nchunk = (hidden + a.chunk_elems - 1) / a.chunk_elems;   // every chunk non-empty
-    a.slot_batch = kSlotBatchInts / L->R;
-    if (a.slot_batch < 1) a.slot_batch = 1;
-    // Channels: by default many short ones (about 2 items each for bf16, 4 for
-    // FP8): each CTA issues the loads of all its items at once, and the
-    // scheduler keeps every SM full while earlier channels drain their stores.
+    // Channels: by default many short ones (one item each for bf16, about 4
+    // for FP8): each CTA issues the loads of all its items at once, and the
+    // scheduler keeps every SM full while earlier channels drain their stores
+    // (measured on GB300: one item per channel beats two by ~3 us at the
+    // DeepSeek-V3 shape).
     const int64_t n_items = static_cast<int64_t>(L->T) * a.nchunk;
-    int64_t grid = num_channels > 0 ? num_channels : (n_items + (fp8 ? 3 : 1)) / (fp8 ? 4 : 2);
+    int64_t grid = num_channels > 0 ? num_channels : (fp8 ? (n_items + 3) / 4 : n_items);
     if (grid > n_items) grid = n_items;
     if (grid < 1) grid = 1;
     const int64_t items_per_channel = (n_items + grid - 1) / grid;
     int S = stages > 0 ? stages : (fp8 ? 3 : 4);
     if (S > items_per_channel) S = static_cast<int>(items_per_channel);   // no unused stages
-    if (S < 2) S = 2;
+    // one stage only when every channel holds exactly one item (no refill)
+    if (S < 2 && items_per_channel > 1) S = 2;
     if (S > kMaxStages) S = kMaxStages;
     a.stages = S;
+    // recv_slot rows staged per batch: at most the tokens one channel spans
+    int64_t slot_tokens = items_per_channel / a.nchunk + 2;
+    if (slot_tokens > kSlotBatchInts / L->R) slot_tokens = kSlotBatchInts / L->R;
+    a.slot_batch = slot_tokens < 1 ? 1 : static_cast<int32_t>(slot_tokens);
 
     size_t smem = align_up(8 * kMaxStages + sizeof(int32_t) * static_cast<size_t>(a.slot_batch) * a.R, 128);
     if (fp8) {
