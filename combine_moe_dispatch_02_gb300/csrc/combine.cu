@@ -113,6 +113,8 @@ combine_kernel(CombineArgs a) {
     if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
 }
 
+constexpr int kCombineWaves = 4;
+
 template <int KT>
 cudaError_t launch_k(const CombineArgs& a, cudaStream_t stream, int32_t num_channels) {
     const int64_t n_items = static_cast<int64_t>(a.T) * a.H8;
@@ -120,7 +122,10 @@ cudaError_t launch_k(const CombineArgs& a, cudaStream_t stream, int32_t num_chan
     cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, combine_kernel<KT>, kCombineThreads, 0);
     if (err != cudaSuccess) return err;
     if (per_sm < 1) per_sm = 1;
-    int64_t grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm;
+    // four waves of resident CTAs by default: on GB300 (the whole step, three
+    // full-size shapes) faster than one persistent wave and than one item per
+    // thread, or within noise of the better of the two
+    int64_t grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm * kCombineWaves;
     const int64_t need = (n_items + kCombineThreads - 1) / kCombineThreads;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
