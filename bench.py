@@ -468,7 +468,10 @@ def run_ours(args, rank, world, local_rank):
 def run_e2e(args, inp, L, dev, ab, step_bytes):
     """Same step through the public API with host buffers: pinned host ->
     device copies of the inputs, the three calls, device -> host copy of the
-    combine output and the per-expert counts, all inside the timed region."""
+    combine output and the per-expert counts, every step inside the timed
+    region.  Two device buffer sets: the inputs of step i+1 are copied on a
+    copy stream while step i computes and copies its result back, as a
+    serving or training loop would overlap them."""
     import torch
     from combine_moe_dispatch_02_gb300 import ep
     wl = inp.wl
@@ -478,40 +481,54 @@ def run_e2e(args, inp, L, dev, ab, step_bytes):
     hy = inp.y.pin_memory()
     hout = torch.empty(wl.T, wl.H, dtype=torch.bfloat16).pin_memory()
     hcnt = torch.empty(wl.E, dtype=torch.int32).pin_memory()
-    x = torch.empty_like(inp.x, device=dev)
-    idx = torch.empty_like(inp.topk_idx, device=dev)
-    w = torch.empty_like(inp.topk_w, device=dev)
-    y = torch.empty_like(inp.y, device=dev)
+    bufs = [{"x": torch.empty_like(inp.x, device=dev), "idx": torch.empty_like(inp.topk_idx, device=dev),
+             "w": torch.empty_like(inp.topk_w, device=dev), "y": torch.empty_like(inp.y, device=dev)}
+            for _ in range(2)]
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
     recv, _ = ep.alloc_recv(L, wl.H, False, device=dev)
-    stream = torch.cuda.current_stream(dev)
+    comp = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    copied = [torch.cuda.Event() for _ in range(2)]
+    consumed = [torch.cuda.Event() for _ in range(2)]
     n = max(3, min(args.steps // 10, 50))
 
-    def one():
-        x.copy_(hx, non_blocking=True)
-        idx.copy_(hidx, non_blocking=True)
-        w.copy_(hw, non_blocking=True)
-        y.copy_(hy, non_blocking=True)
-        ep.moe_dispatch_layout(idx, w, wl.E, wl.R, L, stream)
-        ep.moe_dispatch(x, L, False, recv, None, stream)
-        ep.moe_combine(y, L, w, out, stream)
-        hout.copy_(out, non_blocking=True)
-        hcnt.copy_(L.tokens_per_expert, non_blocking=True)
+    def run(steps):
+        for i in range(steps):
+            b = bufs[i % 2]
+            if i >= 2:
+                copy.wait_event(consumed[i % 2])       # step i-2 is done with this buffer set
+            with torch.cuda.stream(copy):
+                b["x"].copy_(hx, non_blocking=True)
+                b["idx"].copy_(hidx, non_blocking=True)
+                b["w"].copy_(hw, non_blocking=True)
+                b["y"].copy_(hy, non_blocking=True)
+            copied[i % 2].record(copy)
+            comp.wait_event(copied[i % 2])
+            ep.moe_dispatch_layout(b["idx"], b["w"], wl.E, wl.R, L, comp)
+            ep.moe_dispatch(b["x"], L, False, recv, None, comp)
+            ep.moe_combine(b["y"], L, b["w"], out, comp)
+            consumed[i % 2].record(comp)
+            hout.copy_(out, non_blocking=True)
+            hcnt.copy_(L.tokens_per_expert, non_blocking=True)
 
-    for _ in range(3):
-        one()
+    run(3)
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(n):
-        one()
-    e1.record(stream)
+    e0.record(comp)
+    copy.wait_event(e0)
+    run(n)
+    comp.wait_stream(copy)
+    e1.record(comp)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / n
+    st, _ = ep.moe_layout_read_status(L, comp)
+    if st != 0:
+        raise RuntimeError(f"device status {st} in the end-to-end leg")
     h2d = hx.numel() * 2 + hidx.numel() * 4 + hw.numel() * 4 + hy.numel() * 2
     d2h = hout.numel() * 2 + hcnt.numel() * 4
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
+            "overlap": "inputs of step i+1 copied while step i computes (two device buffer sets)"}
 
 
 # ------------------------------------------------------------ CPU baselines

@@ -62,8 +62,12 @@ typedef enum moe_status {
 
 /* Optional launch tuning; pass NULL for the defaults. */
 typedef struct moe_tuning {
-    int32_t  num_channels;     /* CTAs ("independent channels") for dispatch / combine; 0 = auto  */
-    int32_t  stages;           /* dispatch pipeline depth per channel, 2..8; 0 = auto             */
+    int32_t  num_channels;     /* CTAs ("independent channels") for dispatch / combine; 0 = auto
+                                  (bf16 dispatch: one (token, chunk) item per CTA; vector
+                                  dispatch and combine: four waves of resident CTAs)            */
+    int32_t  stages;           /* dispatch pipeline depth per channel, 2..8; 0 = auto (TMA
+                                  kernels: at most the items a channel holds; variant 2: 2 / 4 / 8
+                                  = batches of 1 / 2 / 4 items, two batches in flight)          */
     int32_t  chunk_bytes;      /* dispatch: bf16 bytes of a row per pipeline item (a multiple of
                                   256, >= 256); 0 = 16384, i.e. whole rows up to hidden 8192     */
     int32_t  variant;          /* dispatch / combine kernel: 0 = default (bf16 dispatch: 1;
