@@ -148,7 +148,7 @@ def test_tuning_variants_agree():
     wl = WORKLOADS["dsv3"].scaled(512)
     inp = make_inputs(wl)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R)
-    for ch, st, cb, var in [(1, 2, 0, 1), (4, 3, 2048, 1), (16, 8, 4096, 1), (1000, 0, 0, 1),
+    for ch, st, cb, var in [(1, 2, 0, 1), (4, 3, 2048, 1), (16, 8, 4096, 1), (1000, 0, 0, 1), (100000, 0, 2048, 1),
                             (1, 0, 0, 2), (5, 0, 0, 2), (3000, 0, 0, 2), (0, 4, 0, 2), (7, 4, 0, 2), (0, 8, 0, 2),
                             (5, 2, 0, 2)]:
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, num_channels=ch, stages=st,
@@ -157,7 +157,8 @@ def test_tuning_variants_agree():
     o8 = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True)
     for ch, st, cb, var in [(1, 2, 0, 1), (7, 4, 2048, 1), (3, 0, 0, 2), (999, 0, 0, 2),
                             (1, 0, 0, 3), (7, 0, 2048, 3), (999, 0, 4096, 3), (0, 4, 0, 2), (9, 4, 0, 2),
-                            (0, 8, 0, 2), (3, 2, 0, 2)]:
+                            (0, 8, 0, 2), (3, 2, 0, 2),
+                            (100000, 0, 0, 1), (100000, 0, 2048, 1)]:     # one item per channel: one stage
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True, num_channels=ch, stages=st,
                     chunk_bytes=cb, variant=var)
         assert_parity(g, o8, fp8=True)
