@@ -44,6 +44,10 @@ namespace {
 // entries with one shared-memory atomicMin per entry; larger ones (many ranks)
 // compare every entry with the token's other entries.
 constexpr int kMaxPrimSlots = 16384;
+// Experts up to this count find equal ids in a warp with a shared-memory
+// table of lane masks (one atomicOr per lane); more experts take one ballot
+// per bit of the id.
+constexpr int kMaxPeerE = 256;
 constexpr int kFinalizePerThread = kFinalizeTokens * MOE_MAX_TOPK / kFinalizeThreads;   // entries per thread (4)
 static_assert(kFinalizePerThread * kFinalizeThreads == kFinalizeTokens * MOE_MAX_TOPK,
               "a finalize block's threads cover its 32 tokens' entries for every K <= MOE_MAX_TOPK");
@@ -133,6 +137,8 @@ layout_scan_kernel(ScanArgs a) {
     int4* s_part = reinterpret_cast<int4*>(s_agg + W);                // [kLayoutThreads]
     int32_t* s_rank = reinterpret_cast<int32_t*>(s_part + kLayoutThreads);   // [E]
     int32_t* s_min = s_rank + a.E;    // [tile_tokens][R] if prim_table: min of (e << 5 | k) per (token, rank)
+    const bool peer_table = a.E <= kMaxPeerE;
+    uint32_t* s_peer = reinterpret_cast<uint32_t*>(s_min + (a.prim_table ? a.tile_tokens * a.R : 0));   // [warps][kMaxPeerE]
     __shared__ int s_tile;
     __shared__ uint32_t s_gen;
     __shared__ int s_lb_count, s_lb_final;
@@ -149,6 +155,8 @@ layout_scan_kernel(ScanArgs a) {
     for (int e = tid; e < a.E; e += kLayoutThreads) s_rank[e] = e / a.m;
     if (a.prim_table)
         for (int i = tid; i < a.tile_tokens * a.R; i += kLayoutThreads) s_min[i] = INT_MAX;
+    if (peer_table)
+        for (int i = tid; i < kLayoutWarps * kMaxPeerE; i += kLayoutThreads) s_peer[i] = 0u;
     __syncthreads();
     const int tile = s_tile;
     const uint32_t gen = s_gen;
@@ -219,9 +227,10 @@ layout_scan_kernel(ScanArgs a) {
     }
 
     // 2. order-preserving ranks inside the tile: each warp keeps its own
-    //    histogram.  Lanes with the same expert are found with one ballot per
-    //    bit of the expert id.
-    const int nbits = 32 - __clz(max(a.E - 1, 1));
+    //    histogram.  Lanes with the same expert (peers) come from a table of
+    //    lane masks (each lane ORs its bit into its expert's word, reads the
+    //    word back, clears it), or, for many experts, from one ballot per bit
+    //    of the expert id.  Masked lanes count as peers of each other.
     int lr_e[kMaxChunksPerWarp], lr_p[kMaxChunksPerWarp], ent_e[kMaxChunksPerWarp];
     int32_t* my_hist = s_hist + warp * W;
     uint32_t peers[kMaxChunksPerWarp];
@@ -232,12 +241,28 @@ layout_scan_kernel(ScanArgs a) {
         if (key[c] < 0) peers[c] = ~peers[c];
         rpeers[c] = peers[c];
     }
-    for (int b = 0; b < nbits; ++b) {
+    if (peer_table) {
+        uint32_t* tbl = s_peer + warp * kMaxPeerE;
 #pragma unroll
         for (int c = 0; c < kMaxChunksPerWarp; ++c) {
-            const bool bit = (key[c] >> b) & 1;
-            const uint32_t bb = __ballot_sync(0xffffffffu, bit);
-            peers[c] &= bit ? bb : ~bb;
+            const bool valid = key[c] >= 0;
+            const int e = key[c] & 0xffff;
+            if (valid) atomicOr(&tbl[e], 1u << lane);
+            __syncwarp();
+            if (valid) peers[c] = tbl[e];
+            __syncwarp();
+            if (valid) tbl[e] = 0u;
+            __syncwarp();
+        }
+    } else {
+        const int nbits = 32 - __clz(max(a.E - 1, 1));
+        for (int b = 0; b < nbits; ++b) {
+#pragma unroll
+            for (int c = 0; c < kMaxChunksPerWarp; ++c) {
+                const bool bit = (key[c] >> b) & 1;
+                const uint32_t bb = __ballot_sync(0xffffffffu, bit);
+                peers[c] &= bit ? bb : ~bb;
+            }
         }
     }
     if constexpr (SRC) {
@@ -681,6 +706,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     const bool src = L->num_sources > 0;
     size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
                                       static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
+    if (L->E <= kMaxPeerE) smem1 += sizeof(uint32_t) * kLayoutWarps * kMaxPeerE;   // lane-mask tables
     const size_t table_bytes = sizeof(int32_t) * static_cast<size_t>(L->tile_tokens) * L->R;
     sa.prim_table = (static_cast<int64_t>(L->tile_tokens) * L->R <= kMaxPrimSlots &&
                      smem1 + table_bytes <= kMaxSmemPerBlock) ? 1 : 0;
