@@ -101,6 +101,7 @@ __device__ __forceinline__ int div_small(int i, float inv_k) {
 
 constexpr uint32_t kWaitTimedOut = 4u;
 constexpr int kLookbackWindow = 32;      // predecessors one look-back step inspects (warp 0's lanes)
+constexpr int kTaggedBatch = 16;         // tagged words a thread loads at once (one round for <= 16 predecessors)
 
 // Wait (bounded) until a tile flag carries generation `gen`; return its state,
 // kFlagError if another CTA aborted the scan, or kWaitTimedOut.
@@ -215,15 +216,26 @@ layout_scan_kernel(ScanArgs a) {
 
     // 1c. publish the tile aggregate now, so that successors find it on their
     //     first look-back poll; tile 0's aggregate is its inclusive prefix
-    //     (the barrier orders every thread's stores before thread 0's fence
-    //     and release store, which publish them at GPU scope)
     const bool stall = (a.debug_flags & MOE_DEBUG_STALL_FIRST_TILE) && tile == 0;
-    int32_t* my_vec = (tile == 0 ? a.ws.tile_incl : a.ws.tile_agg) + static_cast<int64_t>(tile) * W;
-    for (int col = tid; col < W; col += kLayoutThreads) my_vec[col] = s_agg[col];
-    __syncthreads();
-    if (tid == 0 && !stall) {
-        __threadfence();
-        st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | (tile == 0 ? kFlagPrefix : kFlagAgg));
+    // With at most 33 tiles every look-back sums all its predecessors'
+    // aggregates, published as generation-tagged 64-bit words: no fence, no
+    // flag, and a reader validates each word it loads.  More tiles: vectors
+    // plus a progress flag (the barrier orders every thread's stores before
+    // thread 0's fence and release store, which publish them at GPU scope).
+    const bool tagged = a.num_tiles <= kLookbackWindow + 1;
+    if (tagged) {
+        uint64_t* my_words = a.ws.tile_tagged + static_cast<int64_t>(tile) * W;
+        if (!stall)
+            for (int col = tid; col < W; col += kLayoutThreads)
+                st_relaxed_gpu_u64(my_words + col, (static_cast<uint64_t>(gen) << 32) | static_cast<uint32_t>(s_agg[col]));
+    } else {
+        int32_t* my_vec = (tile == 0 ? a.ws.tile_incl : a.ws.tile_agg) + static_cast<int64_t>(tile) * W;
+        for (int col = tid; col < W; col += kLayoutThreads) my_vec[col] = s_agg[col];
+        __syncthreads();
+        if (tid == 0 && !stall) {
+            __threadfence();
+            st_release_gpu(&a.ws.tile_flag[tile], (gen << 2) | (tile == 0 ? kFlagPrefix : kFlagAgg));
+        }
     }
 
     // 2. order-preserving ranks inside the tile: each warp keeps its own
@@ -321,7 +333,44 @@ layout_scan_kernel(ScanArgs a) {
     // 4. decoupled look-back over the predecessors' aggregates and inclusive
     //    prefixes
     bool failed = false;
-    if (tile > 0) {
+    if (tile > 0 && tagged) {
+        // every thread sums its own columns over all predecessors: one round of
+        // loads, a bounded re-load of any word whose tag is not yet current
+        bool tmo = false, aborted = false;
+        for (int col = tid; col < W && !tmo && !aborted; col += kLayoutThreads) {
+            int32_t sum = 0;
+            for (int q0 = 0; q0 < tile && !tmo && !aborted; q0 += kTaggedBatch) {
+                uint64_t v[kTaggedBatch];
+#pragma unroll
+                for (int u = 0; u < kTaggedBatch; ++u)
+                    v[u] = q0 + u < tile ? ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(q0 + u) * W + col)
+                                         : (static_cast<uint64_t>(gen) << 32);
+#pragma unroll
+                for (int u = 0; u < kTaggedBatch; ++u) {
+                    uint64_t t0 = 0;
+                    for (uint32_t it = 0; static_cast<uint32_t>(v[u] >> 32) != gen; ++it) {
+                        if (ld_relaxed_gpu(&a.ws.hdr->abort) == gen) { aborted = true; break; }
+                        if (it == 0) {
+                            t0 = globaltimer_ns();
+                        } else if (globaltimer_ns() - t0 > a.timeout_ns) {
+                            tmo = true;
+                            break;
+                        }
+                        __nanosleep(it < 32 ? 32 : 256);
+                        v[u] = ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(q0 + u) * W + col);
+                    }
+                    if (tmo || aborted) break;
+                    sum += static_cast<int32_t>(static_cast<uint32_t>(v[u]));
+                }
+            }
+            s_prefix[col] = sum;
+        }
+        if (tmo) {
+            atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_TIMEOUT);
+            atomicExch(&a.ws.hdr->abort, gen);
+        }
+        if (__syncthreads_or(tmo || aborted)) return;
+    } else if (tile > 0) {
         // the window's vectors are summed by `groups` thread groups, each taking
         // every groups-th predecessor, with 16-byte loads: one round of loads
         const int groups = max(1, min(8, kLayoutThreads / nvec));
@@ -401,11 +450,10 @@ layout_scan_kernel(ScanArgs a) {
 
     // 6. the inclusive prefix.  The last tile's is the totals vector the
     //    finalize pass reads (kernel completion publishes it).  Other tiles
-    //    publish theirs only when a look-back can need it: with at most 33
-    //    tiles every look-back window reaches tile 0, whose prefix is published
-    //    with its aggregate.
-    const bool flagged = a.num_tiles > kLookbackWindow + 1;
-    if (tile > 0 && (flagged || tile == a.num_tiles - 1)) {
+    //    publish theirs, with a flag, only when look-backs use flags (more
+    //    than 33 tiles).
+    const bool flagged = !tagged && tile > 0;     // (with flags, tile 0 published its prefix above)
+    if (flagged || tile == a.num_tiles - 1) {
         int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * W;
         for (int col = tid; col < W; col += kLayoutThreads) my_incl[col] = s_prefix[col] + s_agg[col];
         if (flagged) {
@@ -671,6 +719,7 @@ size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles
     b = align_up(b + sizeof(uint32_t) * num_tiles, 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * vec_width(E), 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * vec_width(E), 256);
+    b = align_up(b + sizeof(uint64_t) * static_cast<size_t>(min(num_tiles, kLookbackWindow + 1)) * vec_width(E), 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
     return b;
@@ -688,6 +737,9 @@ LayoutWs layout_workspace(const moe_layout* L) {
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * vec_width(L->E), 256);
     ws.tile_incl = reinterpret_cast<int32_t*>(p + off);
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * vec_width(L->E), 256);
+    ws.tile_tagged = reinterpret_cast<uint64_t*>(p + off);
+    off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(min(L->num_tiles, kLookbackWindow + 1)) *
+                             vec_width(L->E), 256);
     ws.erank = reinterpret_cast<int32_t*>(p + off);
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->T) * L->K, 256);
     ws.prank = reinterpret_cast<int32_t*>(p + off);

@@ -36,6 +36,8 @@ struct LayoutWs {
     uint32_t* tile_flag;   // [num_tiles]: (generation << 2) | state
     int32_t*  tile_agg;    // [num_tiles][2E]: this tile's counts (expert, primary)
     int32_t*  tile_incl;   // [num_tiles][2E]: counts of tiles 0..i inclusive
+    uint64_t* tile_tagged; // [min(num_tiles, 33)][2E]: (generation << 32) | count, the aggregates
+                           // of the look-back without flags (at most 33 tiles)
     int32_t*  erank;       // [T*K]: rank of entry among entries of its expert
     int32_t*  prank;       // [T*K]: rank of a primary entry among its expert's primaries
 };
@@ -72,6 +74,19 @@ __device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
 
 __device__ __forceinline__ void st_release_gpu(uint32_t* p, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+// 64-bit accesses are single-copy atomic: a reader sees either the old or the
+// new word, never a mix, so a generation tag in the upper half validates the
+// count in the lower half.
+__device__ __forceinline__ uint64_t ld_relaxed_gpu_u64(const uint64_t* p) {
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed_gpu_u64(uint64_t* p, uint64_t v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" :: "l"(p), "l"(v) : "memory");
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
