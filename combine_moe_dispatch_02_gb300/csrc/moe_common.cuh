@@ -182,9 +182,6 @@ __device__ __forceinline__ void bulk_wait_read_n(int n) {
     }
 }
 
-// Wait until all of this thread's bulk groups have completed.
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
 // Order this thread's generic-proxy shared-memory accesses before later
 // async-proxy (TMA) accesses.
 __device__ __forceinline__ void fence_proxy_async_smem() {
