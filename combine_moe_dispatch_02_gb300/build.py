@@ -36,14 +36,17 @@ def _inputs_mtime() -> float:
 def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = False) -> str:
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= _inputs_mtime():
         return LIB_PATH
-    os.makedirs(BUILD_DIR, exist_ok=True)
+    # objects in a directory of this process: concurrent builds (one per rank)
+    # never share a file; the library itself is replaced atomically
+    obj_dir = os.path.join(BUILD_DIR, f"p{os.getpid()}")
+    os.makedirs(obj_dir, exist_ok=True)
     common = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-Wall",
               "-I", INCLUDE, "-I", CSRC]
     if ptxas_verbose:
         common += ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> tuple[str, str]:
-        obj = os.path.join(BUILD_DIR, src.replace(".cu", ".o"))
+        obj = os.path.join(obj_dir, src.replace(".cu", ".o"))
         cmd = common + ["-c", os.path.join(CSRC, src), "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -62,6 +65,7 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB_PATH)
+    shutil.rmtree(obj_dir, ignore_errors=True)
     return LIB_PATH
 
 
