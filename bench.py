@@ -38,9 +38,19 @@ L2_FLUSH_BYTES = 256 << 20
 
 # Secondary legs run after the timed step (each reported under "ops"); the
 # headline step and its layout / dispatch split always run.
-LEGS = ("fp8", "mxfp8", "backward", "ll", "sources", "channels", "e2e")
+LEGS = ("fp8", "mxfp8", "backward", "ll", "sources", "workloads", "channels", "e2e")
+# the other routing shapes, measured as an eager flushed step each (secondary figures)
+OTHER_WORKLOADS = ("qwen_skew", "ds16_wide")
 # CTA counts of the channel sweep (the pages fill NVLink with 4 SMs; HBM needs many more)
 SWEEP_CTAS = (4, 8, 16, 32, 64, 152, 304, 608, 1216)
+
+
+def workload_label(wl):
+    """What the workload is, with its sizes."""
+    kind = {"dsv3": "DeepSeek-V3 shape", "dsv3_fp8": "DeepSeek-V3 shape",
+            "qwen_skew": "Qwen3-235B-like shape, Zipf-skewed routing",
+            "ds16_wide": "DeepSeek-16B-like shape over 32 ranks", "tiny": "toy shape"}.get(wl.name, wl.name)
+    return (f"{kind}: {wl.T} tokens, hidden {wl.H}, {wl.E} experts / {wl.R} virtual ranks, top-{wl.K}")
 
 
 def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
@@ -407,6 +417,47 @@ def run_ours(args, rank, world, local_rank):
                                   "combine": hbm_op(msc, ab_ms["combine"])}
         del x_ms, y_ms, recv_ms, out_ms, L_ms
 
+    # the other routing shapes: Zipf-skewed Qwen3-235B-like routing (one rank
+    # receives nearly every token) and DeepSeek-16B-like routing over 32 ranks
+    # with a narrow hidden size; each an eager flushed step of its own
+    if "workloads" in legs:
+        wls = {}
+        for name in OTHER_WORKLOADS:
+            if name == args.workload:
+                continue
+            wo = WORKLOADS[name]
+            To, Ho, Eo, Ro, Ko = wo.T, wo.H, wo.E, wo.R, wo.K
+            inp_o = make_inputs(wo, seed=rank, with_y=False)
+            L_o = ep.Layout(To, Ko, Eo, Ro, device=dev)
+            x_o, idx_o, w_o = inp_o.x.to(dev), inp_o.topk_idx.to(dev), inp_o.topk_w.to(dev)
+            gen = torch.Generator(device=dev).manual_seed(99 + rank)
+            y_o = torch.randn(To * Ko, Ho, device=dev, generator=gen).to(torch.bfloat16)
+            recv_o, _ = ep.alloc_recv(L_o, Ho, False, device=dev)
+            out_o = torch.empty(To, Ho, dtype=torch.bfloat16, device=dev)
+
+            def body(e):
+                e[0].record(stream)
+                ep.moe_dispatch_layout(idx_o, w_o, Eo, Ro, L_o, stream)
+                e[1].record(stream)
+                ep.moe_dispatch(x_o, L_o, False, recv_o, None, stream)
+                e[2].record(stream)
+                ep.moe_combine(y_o, L_o, w_o, out_o, stream)
+                e[3].record(stream)
+            ol, od, oc = timed(body, n_sec, 4)
+            st, flags = ep.moe_layout_read_status(L_o, stream)
+            if st != 0:
+                raise RuntimeError(f"device status {st} in the {name} leg")
+            tpr = L_o.tokens_per_rank.cpu()
+            ab_o = algorithmic_bytes(To, Ho, Eo, Ro, Ko, int(tpr.sum()), int(L_o.expert_offset[Eo].item()),
+                                     L_o.capacity)
+            wls[name] = {"shape": workload_label(wo), "n_pairs": int(tpr.sum()),
+                         "rows_per_rank_min_max": [int(tpr.min()), int(tpr.max())],
+                         "layout_us": round(ol * 1e3, 2),
+                         "dispatch_bf16": hbm_op(od, ab_o["dispatch"], tokens_per_s=round(To / (od * 1e-3), 1)),
+                         "combine": hbm_op(oc, ab_o["combine"], tokens_per_s=round(To / (oc * 1e-3), 1))}
+            del x_o, y_o, recv_o, out_o, L_o
+        ops["other_workloads"] = wls
+
     # how many CTAs ("channels") the HBM-bound operators need: bf16 dispatch (one
     # warp per CTA) and combine (256 threads per CTA) at fixed CTA counts
     if "channels" in legs:
@@ -441,15 +492,16 @@ def run_ours(args, rank, world, local_rank):
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": "bf16",
-        "data": "synthetic (seeded N(0,1) activations, softmax top-8 routing of N(0,1) logits)",
-        "config": {"workload": "DeepSeek-V3 shape: 4096 tokens, hidden 7168, 256 experts / 8 virtual ranks, top-8",
+        "data": f"synthetic (seeded N(0,1) activations, softmax top-{K} routing of N(0,1) logits"
+                + (f", Zipf s={wl.zipf_s} expert bias)" if wl.zipf_s else ")"),
+        "config": {"workload": workload_label(wl),
                    "T": T, "H": H, "E": E, "R": R, "K": K, "n_pairs": n_pairs, "capacity": L.capacity,
                    "step": "layout + bf16 dispatch + combine", "l2": "flushed between steps (256 MB write, then 256 MB read of another buffer)",
                    "launch": "timed steps replay one CUDA graph (layout -> dispatch -> combine)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "ops": ops,
-        "roofline": {"bound": "hbm", "kernel": "combine_kernel<8>", "achieved": round(achieved, 1),
+        "roofline": {"bound": "hbm", "kernel": f"combine_kernel<{K if K in (1, 2, 4, 6, 8) else 0}>", "achieved": round(achieved, 1),
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
