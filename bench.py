@@ -505,7 +505,8 @@ def run_ours(args, rank, world, local_rank):
                      "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
                      else "fallback 6.8 TB/s",
-                     "traffic": committed_traffic("combine.cu", "combine_dsv3_ncu.md"),
+                     "traffic": committed_traffic("combine.cu", "combine_dsv3_ncu.md") if args.workload == WORKLOAD
+                     else None,
                      "timing": "combine between events in the eager per-operator pass, after the dispatch",
                      "algorithmic_bytes": ab["combine"]},
         "gpu_launches": 4 * args.steps,

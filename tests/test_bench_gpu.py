@@ -1,0 +1,62 @@
+"""bench.py on the GPU: one short run of the full-size step with the
+end-to-end leg, checked for the keys and units of its JSON line (the
+timed-region contract: warm-up and step counts, the roofline of the
+dominant kernel, clocks, the end-to-end figure and the launch count)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _run(*extra):
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "5", "--warmup", "3",
+           "--no-cpu-baseline", *extra]
+    r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout[-2000:]
+    return json.loads(lines[0])
+
+
+def test_bench_json_line_contract():
+    d = _run("--legs", "e2e")
+    assert d["unit"] == "GB/s" and d["higher_is_better"] is True and d["scaling"] == "weak"
+    assert d["n_gpus"] == 1 and d["steps"] == 5 and d["warmup"] == 3
+    assert d["value"] > 0 and d["ms_per_step"] > 0 and d["vs_baseline"] is None
+    assert d["dtype"] == "bf16" and d["data"].startswith("synthetic")
+    cfg = d["config"]
+    assert "4096 tokens, hidden 7168, 256 experts / 8 virtual ranks, top-8" in cfg["workload"]
+    assert (cfg["T"], cfg["H"], cfg["E"], cfg["R"], cfg["K"]) == (4096, 7168, 256, 8, 8)
+    assert "flushed" in cfg["l2"]
+    # the step's bytes / time is the value; the value is the layout + dispatch + combine bytes
+    rf = d["roofline"]
+    assert rf["bound"] == "hbm" and rf["unit"] == "GB/s" and rf["kernel"] == "combine_kernel<8>"
+    assert rf["peak"] > 0 and abs(rf["frac"] - rf["achieved"] / rf["peak"]) < 1e-3
+    assert 0.3 < rf["frac"] < 1.5
+    assert rf["traffic"] is None or rf["traffic"] > 0.5 * rf["algorithmic_bytes"]
+    e2e = d["e2e"]
+    assert e2e["unit"] == "GB/s" and 0 < e2e["value"] < d["value"]
+    assert e2e["h2d_bytes_per_step"] > 0 and e2e["d2h_bytes_per_step"] > 0
+    assert d["gpu_launches"] == 4 * d["steps"]
+    clk = d["clocks"]
+    assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+    ops = d["ops"]
+    for key in ("layout", "dispatch_bf16", "combine"):
+        assert ops[key]["us"] > 0
+    for key in ("dispatch_bf16", "combine"):
+        assert ops[key]["bytes"] > 0 and 0.2 < ops[key]["frac"] < 1.5
+
+
+def test_bench_other_workload_as_the_step():
+    d = _run("--legs", "none", "--workload", "ds16_wide")
+    cfg = d["config"]
+    assert (cfg["T"], cfg["H"], cfg["E"], cfg["R"], cfg["K"]) == (16384, 2048, 64, 32, 6)
+    assert "32 ranks" in cfg["workload"] and d["roofline"]["kernel"] == "combine_kernel<6>"
+    assert d["value"] > 0 and "e2e" not in d
+    assert d["roofline"]["traffic"] is None            # the committed capture is of the DeepSeek-V3 shape
