@@ -64,6 +64,24 @@ def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed, variant):
     assert_parity(g, o, fp8=fp8)
 
 
+@pytest.mark.parametrize("T,H,E,R,K,mask,fp8,seed", [
+    (262144, 8, 256, 8, 8, 0.0, False, 20),    # 1,024 scan tiles: the flag look-back at length
+    (100003, 16, 64, 4, 6, 0.05, False, 21),   # ragged last tile, masked entries
+    (65536, 128, 256, 8, 8, 0.0, True, 22),    # FP8 over 256 tiles
+])
+def test_large_token_counts(T, H, E, R, K, mask, fp8, seed):
+    idx = random_routing(T, K, E, seed, mask_frac=mask)
+    w = random_weights(T, K, seed)
+    g_ = torch.Generator().manual_seed(seed + 1)
+    x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
+    y = torch.randn(T * K, H, generator=g_).to(torch.bfloat16)
+    g = gpu_run(x, idx, w, y, E, R, fp8=fp8)
+    o = oracle_run(x, idx, w, y, E, R, fp8=fp8)
+    assert g["status"] == 0 and o["status"] == 0
+    assert_parity(g, o, fp8=fp8)
+    assert np.array_equal(g["out"], o["out"])
+
+
 def test_zero_tokens():
     E, R, K, H = 8, 2, 2, 64
     idx = torch.zeros(0, K, dtype=torch.int32)
