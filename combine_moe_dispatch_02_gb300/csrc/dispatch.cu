@@ -587,8 +587,14 @@ __device__ __forceinline__ void lsu_store(const LsuBatch<U>& b, const DispatchAr
 // Software-pipelined in batches of U items per warp: the next batch's loads
 // are issued before the current batch is quantised and stored, so the load
 // latency overlaps the arithmetic and the stores (2U items in flight).
+// Registers for U = 1 (the default): MXFP8 is held to five CTAs per SM (48
+// registers, 4 bytes of spill), which on GB300 beat four CTAs (60 registers) by
+// 0.5-1.0 us on all three full-size shapes; FP8 and bf16 are held to four (FP8:
+// 64 registers, as fast as before; at five it spills 16 bytes and measured up
+// to 0.8 us slower).  Deeper batches keep their registers (bounded to four or
+// five CTAs they spill hundreds of bytes).
 template <int FMT, int U>
-__global__ void __launch_bounds__(kLsuThreads)
+__global__ void __launch_bounds__(kLsuThreads, U == 1 ? (FMT == 2 ? 5 : 4) : 1)
 dispatch_lsu_kernel(DispatchArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
