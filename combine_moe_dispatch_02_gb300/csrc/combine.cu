@@ -181,6 +181,7 @@ combine_tma_kernel(CombineArgs a, uint64_t timeout_ns) {
     }
     __syncthreads();
     bool bad = false, timed_out = false;
+    int issued = 0;                                 // producer: items whose loads were posted
 
     if (warp == 0) {
         // ---------------- producer
@@ -215,6 +216,7 @@ combine_tma_kernel(CombineArgs a, uint64_t timeout_ns) {
                 bulk_g2s(stage0 + s * stage_bytes + static_cast<size_t>(lane) * kTmaCE * 2,
                          reinterpret_cast<const uint8_t*>(a.y) + (static_cast<int64_t>(slot) * H + c * kTmaCE) * 2,
                          bytes, &full[s]);
+            ++issued;
         }
     } else {
         // ---------------- consumers
@@ -246,9 +248,13 @@ combine_tma_kernel(CombineArgs a, uint64_t timeout_ns) {
             }
         }
     }
+    // after a timeout on either side, the producer waits (bounded) for the
+    // loads it posted before the CTA's shared memory goes away
+    const bool any_timeout = __syncthreads_or(timed_out);
+    if (any_timeout && warp == 0) drain_ring_loads(full, kTmaStages, issued, timeout_ns);
     pdl_trigger();
     if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
-    if (__syncthreads_or(timed_out) && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
+    if (any_timeout && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
 }
 
 }  // namespace

@@ -109,6 +109,7 @@ dispatch_bf16_kernel(DispatchArgs a) {
     if (lane == 0) {
         for (int k = 0; k < S && k < rg.n; ++k) issue_load(k);
     }
+    int issued = min(S, rg.n);                  // warp-uniform
 
     const int64_t last_token = (rg.i0 + rg.n - 1) / a.nchunk;
     int64_t batch_t0 = 0, batch_t1 = -1;
@@ -146,12 +147,15 @@ dispatch_bf16_kernel(DispatchArgs a) {
             bulk_wait_read<1>();
             __syncwarp();
             if (lane == 0) issue_load(k - 1 + S);
+            ++issued;
         }
     }
     pdl_trigger();          // many waves: let the next kernel launch only as channels finish
-    // Exit once the stores have read the stages: the shared memory goes away
-    // with the CTA, while kernel completion makes the global writes visible.
+    // Exit once the stores have read the stages (and, after a timeout, once
+    // the loads still in flight have landed): the shared memory goes away with
+    // the CTA, while kernel completion makes the global writes visible.
     bulk_wait_read<0>();
+    if (timed_out) drain_ring_loads(bars, S, issued, a.timeout_ns);
     const uint32_t any_bad = __ballot_sync(0xffffffffu, bad);
     const uint32_t any_tmo = __ballot_sync(0xffffffffu, timed_out);
     if (lane == 0) {
@@ -210,6 +214,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
     if (tid == 0) {
         for (int k = 0; k < S && k < rg.n; ++k) issue_load(k);
     }
+    int issued = min(S, rg.n);                  // CTA-uniform
 
     const int64_t last_token = (rg.i0 + rg.n - 1) / a.nchunk;
     int64_t batch_t0 = 0, batch_t1 = -1;
@@ -264,7 +269,10 @@ dispatch_fp8_kernel(DispatchArgs a) {
         fence_proxy_async_smem();
         __syncthreads();
         // the input stage is free again: fetch item k+S into it
-        if (tid == 0 && k + S < rg.n) issue_load(k + S);
+        if (k + S < rg.n) {
+            if (tid == 0) issue_load(k + S);
+            ++issued;
+        }
         const int32_t* trow = s_slots + (t - batch_t0) * a.R;
         if (warp == 0) {
             for (int r = lane; r < a.R; r += 32) {
@@ -285,6 +293,7 @@ dispatch_fp8_kernel(DispatchArgs a) {
     }
     pdl_trigger();
     if (warp == 0) bulk_wait_read<0>();     // stages read; completion publishes the writes
+    if (timed_out) drain_ring_loads(bars, S, issued, a.timeout_ns);   // loads still in flight
     if (__syncthreads_or(bad) && tid == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
     if (timed_out && tid == 0) atomicOr(a.status, MOE_DEVERR_TIMEOUT);
 }
@@ -422,11 +431,7 @@ dispatch_fp8_ws_kernel(DispatchArgs a) {
         bulk_wait_read<0>();                 // stages read; completion publishes the writes
         // After a timeout, loads may still be landing in the input ring: wait
         // (bounded) for the last load issued into each stage before exiting.
-        for (int s = 0; s < kWsInStages && s < issued; ++s) {
-            const int j = s + (issued - 1 - s) / kWsInStages * kWsInStages;
-            if (!mbar_wait_bounded(&in_full[s], static_cast<uint32_t>(j / kWsInStages) & 1u, a.timeout_ns))
-                timed_out = true;
-        }
+        if (!drain_ring_loads(in_full, kWsInStages, issued, a.timeout_ns)) timed_out = true;
     } else {
         // ----------------------------------------------------------- quantisers
         const int q = warp - 1;

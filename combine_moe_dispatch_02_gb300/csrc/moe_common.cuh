@@ -144,6 +144,19 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
 }
 
+// After a timed-out wait: wait (bounded) for the last TMA load issued into
+// each stage of a ring whose loads k = 0 .. issued-1 went to stage k % S and
+// complete phase k / S of that stage's mbarrier, so that no load lands in
+// shared memory after the CTA has exited.  False if one is still outstanding.
+__device__ __forceinline__ bool drain_ring_loads(uint64_t* bars, int S, int issued, uint64_t timeout_ns) {
+    bool all = true;
+    for (int s = 0; s < S && s < issued; ++s) {
+        const int j = s + (issued - 1 - s) / S * S;     // the last load issued into stage s
+        all &= mbar_wait_bounded(&bars[s], static_cast<uint32_t>(j / S) & 1u, timeout_ns);
+    }
+    return all;
+}
+
 // TMA bulk copies (non-tensor) -------------------------------------------
 
 // global -> shared, completion signalled as transaction bytes on `bar`.
