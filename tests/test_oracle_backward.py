@@ -53,6 +53,23 @@ def test_dispatch_backward_vs_exact_sum(oracle_lib):
             assert gx[t, h] == bits_of_f32(float(rn_bf16(acc))) >> 16, (t, h)
 
 
+def test_dispatch_backward_sums_in_ascending_rank():
+    """One token on ranks 0, 1 and 2 (one expert per rank) whose receive rows
+    hold 2^24, 1 and -2^24: the fp32 chain in ascending rank order gives
+    (2^24 + 1) - 2^24 = 2^24 - 2^24 = 0 (2^24 + 1 rounds to the even 2^24);
+    descending order gives (-2^24 + 1) + 2^24 = 1."""
+    import oracle
+    oracle.build()
+    L = oracle.layout(np.array([[0, 1, 2]], np.int32), None, 3, 3)
+    H = 8
+    g = np.zeros((L.capacity, H), np.uint16)
+    for r, bits in enumerate((0x4B80, 0x3F80, 0xCB80)):      # bf16 2^24, 1, -2^24
+        g[L.recv_slot[0, r]] = bits
+    gx, st = oracle.dispatch_backward(g, L.recv_slot)
+    assert st == 0
+    assert np.all(gx == 0x0000)
+
+
 def test_combine_backward_grad_y_exact(oracle_lib):
     T, H, E, R, K = 9, 20, 8, 4, 3
     idx = random_routing(T, K, E, 6, mask_frac=0.2).numpy()

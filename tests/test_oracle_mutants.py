@@ -10,9 +10,11 @@ import tempfile
 import pytest
 
 import oracle
+import test_oracle_backward as B
 import test_oracle_codecs as C
 import test_oracle_dispatch_combine as D
 import test_oracle_layout as LY
+import test_oracle_lowlatency as LL
 import test_oracle_sources as SRC
 
 HERE = os.path.dirname(os.path.abspath(oracle.__file__))
@@ -59,6 +61,26 @@ MUTANTS = [
      "for"),
     ("multi-source leaves region tails uncleared",
      "for (int64_t i = 0; i < (int64_t)R * T; ++i) recv_src_token[i] = -1;", ""),
+    ("mxfp8 shared exponent one too large",
+     "shared_exp = (e2 - 1) - 8;", "shared_exp = e2 - 8;"),
+    ("mxfp8 E8M0 bias 128",
+     "recv_scales[slot * nb + b] = (uint8_t)(shared_exp + 127);",
+     "recv_scales[slot * nb + b] = (uint8_t)(shared_exp + 128);"),
+    ("dispatch backward sums ranks in descending order",
+     "for (int32_t r = 0; r < R; ++r) {\n            int64_t row = recv_slot[t * R + r];",
+     "for (int32_t r = R - 1; r >= 0; --r) {\n            int64_t row = recv_slot[t * R + r];"),
+    ("combine backward leaves grad_y unweighted",
+     "float prod = w * g;", "float prod = g;"),
+    ("combine backward weights grad_w",
+     "dot += (double)g * (double)moe_ref_bf16_decode(y[row * H + h]);",
+     "dot += (double)(w * g) * (double)moe_ref_bf16_decode(y[row * H + h]);"),
+    ("low-latency ranks entries by k, then token",
+     "for (int64_t t = 0; t < T; ++t)\n        for (int32_t k = 0; k < K; ++k) {\n            int32_t e = topk_idx[t * K + k];",
+     "for (int32_t k = 0; k < K; ++k)\n        for (int64_t t = 0; t < T; ++t) {\n            int32_t e = topk_idx[t * K + k];"),
+    ("low-latency counts dropped entries",
+     "int32_t j = tokens_per_expert[e];\n                if (j < cap) {\n                    slot = e * cap + j;\n"
+     "                    tokens_per_expert[e] = j + 1;",
+     "int32_t j = tokens_per_expert[e]++;\n                if (j < cap) {\n                    slot = e * cap + j;"),
 ]
 
 
@@ -79,6 +101,15 @@ def _pins():
         ("combine exact chain", lambda: D.test_combine_vs_exact_fma_chain(o)),
         ("combine ascending k", D.test_combine_sums_in_ascending_k),
         ("combine fused", D.test_combine_uses_fused_multiply_add),
+        ("mxfp8 golden", lambda: D.test_mxfp8_golden_values(o)),
+        ("mxfp8 exact pipeline", lambda: D.test_mxfp8_vs_exact_pipeline(o)),
+        ("low-latency golden", lambda: LL.test_ll_worked_example(o)),
+        ("low-latency brute force", lambda: LL.test_ll_vs_brute_force(o, 50, 4, 16, 50, 0.1, False, 0)),
+        ("low-latency overflow", lambda: LL.test_ll_vs_brute_force(o, 20, 3, 4, 8, 0.0, True, 2)),
+        ("dispatch backward exact", lambda: B.test_dispatch_backward_vs_exact_sum(o)),
+        ("dispatch backward ascending r", B.test_dispatch_backward_sums_in_ascending_rank),
+        ("combine backward grad_y exact", lambda: B.test_combine_backward_grad_y_exact(o)),
+        ("combine backward grad_w fp64", lambda: B.test_combine_backward_grad_w_vs_numpy_fp64(o)),
     ]
 
 
