@@ -30,7 +30,7 @@
 // destination, rows in (source, token) order) uses the same two kernels with
 // the primary pairs counted per destination rank instead of per primary
 // expert, and a third, layout_source_offsets_kernel, that reads each source's
-// first row per region off the sorted regions by binary search.
+// first row per region off the sorted regions by a warp-wide 32-way search.
 #include <algorithm>
 #include <climits>
 
@@ -685,23 +685,41 @@ struct SourceOffsetArgs {
     int32_t T, R, S, Ts;
 };
 
+// One warp per (destination r, source s): the first row of region r whose
+// token is at least s * Ts, by a 32-way search.  Each step the lanes probe 32
+// evenly spaced rows of the remaining range; the rows ascend, so the lanes
+// below the target form a prefix and a ballot keeps the gap that holds the
+// boundary: about log32 of the region's length dependent loads, not log2.
 __global__ void __launch_bounds__(256)
 layout_source_offsets_kernel(SourceOffsetArgs a) {
     pdl_wait();
     pdl_trigger();
+    const int lane = threadIdx.x & 31;
     const int64_t n = static_cast<int64_t>(a.R) * (a.S + 1);
-    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
-         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t warps = static_cast<int64_t>(gridDim.x) * (blockDim.x >> 5);
+    for (int64_t i = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; i < n; i += warps) {
         const int r = static_cast<int>(i / (a.S + 1));
         const int s = static_cast<int>(i - static_cast<int64_t>(r) * (a.S + 1));
         const int32_t* rows = a.recv_src_token + static_cast<int64_t>(r) * a.T;
         const int32_t target = s * a.Ts;           // <= T
+        // the first row >= target lies in [lo, hi] (hi: none of the rows is)
         int lo = 0, hi = min(max(a.tokens_per_rank[r], 0), a.T);
-        while (lo < hi) {                          // at most 32 steps
-            const int mid = lo + (hi - lo) / 2;
-            if (rows[mid] < target) lo = mid + 1; else hi = mid;
+        while (hi > lo) {                          // warp-uniform
+            const int len = hi - lo;
+            if (len <= 32) {
+                const bool below = lane < len && rows[lo + lane] < target;
+                lo += __popc(__ballot_sync(0xffffffffu, below));
+                break;
+            }
+            // 32 probes, strictly increasing, in [lo, hi)
+            const int p = lo + static_cast<int>(static_cast<int64_t>(len) * (lane + 1) / 33);
+            const int c = __popc(__ballot_sync(0xffffffffu, rows[p] < target));
+            const int p_below = __shfl_sync(0xffffffffu, p, c > 0 ? c - 1 : 0);
+            const int p_at = __shfl_sync(0xffffffffu, p, c < 32 ? c : 31);
+            if (c > 0) lo = p_below + 1;           // rows[p_below] < target
+            if (c < 32) hi = p_at;                 // rows[p_at] >= target
         }
-        a.recv_source_offset[i] = lo;
+        if (lane == 0) a.recv_source_offset[i] = lo;
     }
 }
 
@@ -799,8 +817,8 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     oa.tokens_per_rank = L->tokens_per_rank;
     oa.recv_source_offset = L->recv_source_offset;
     oa.T = L->T; oa.R = L->R; oa.S = L->num_sources; oa.Ts = L->source_tokens;
-    const int64_t n = static_cast<int64_t>(L->R) * (L->num_sources + 1);
-    const unsigned g3 = static_cast<unsigned>(std::min<int64_t>((n + 255) / 256, 1024));
+    const int64_t n = static_cast<int64_t>(L->R) * (L->num_sources + 1);    // one warp each
+    const unsigned g3 = static_cast<unsigned>(std::min<int64_t>((n + 7) / 8, 1024));
     return launch_pdl(layout_source_offsets_kernel, dim3(g3), dim3(256), 0, stream, oa);
 }
 
