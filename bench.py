@@ -23,6 +23,7 @@ import json
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -123,21 +124,28 @@ class ClockSampler:
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, log_path: str | None = None):
         self.gpu = gpu_index
         self.proc = None
+        self.log_path = log_path        # where to keep the raw samples; a temporary file if None
         self.path = None
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            if self.log_path:
+                os.makedirs(os.path.dirname(os.path.abspath(self.log_path)), exist_ok=True)
+                self.path = self.log_path
+            else:
+                fd, self.path = tempfile.mkstemp(prefix=f"clocks_rank{self.gpu}_", suffix=".csv")
+                os.close(fd)
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+            if self.path and not self.log_path and os.path.exists(self.path):
+                os.unlink(self.path)
 
     def stop(self):
         if self.proc is None:
@@ -162,6 +170,8 @@ class ClockSampler:
             for n, v in zip(names, parts[5:9]):
                 if v.lower() == "active":
                     reasons.add(n)
+        if not self.log_path:
+            os.unlink(self.path)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax,
                 "reasons": sorted(reasons), "samples": len(sm)}
 
@@ -257,7 +267,7 @@ def run_ours(args, rank, world, local_rank):
         evs[1].record(stream)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    sampler = ClockSampler(local_rank)
+    sampler = ClockSampler(local_rank, args.clocks_log.replace("{rank}", str(rank)) if args.clocks_log else None)
     sampler.start()
     time.sleep(0.3)
     if world > 1:
@@ -681,6 +691,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-log", default=None,
+                    help="keep the raw nvidia-smi samples of the timed region here ({rank} is replaced)")
     ap.add_argument("--legs", default="all",
                     help="secondary legs after the timed step: 'all', 'none' or a comma list of " + ",".join(LEGS))
     args = ap.parse_args()
