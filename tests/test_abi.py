@@ -77,6 +77,41 @@ def test_operator_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.moe_combine(None, 64, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
 
 
+def test_more_calls_reject_bad_arguments_on_the_host(lib):
+    """Refusals that happen before anything is enqueued (no GPU needed): the
+    scale buffer rules, tuning outside its ranges, the backward pair and the
+    low-latency calls."""
+    from combine_moe_dispatch_02_gb300 import ep
+    INVALID, UNSUPPORTED = ep.MOE_ERR_INVALID_ARG, ep.MOE_ERR_UNSUPPORTED
+    L = ep.moe_layout()
+    n = ep.moe_layout_bytes(16, 2, 8, 4, 32)
+    assert lib.moe_layout_init(ctypes.byref(L), 16, 2, 8, 4, 32, ctypes.c_void_p(1 << 20), n) == ep.MOE_OK
+    Lp = ctypes.byref(L)
+    p = ctypes.c_void_p(1 << 21)
+    off4 = ctypes.c_void_p((1 << 21) + 4)        # 4-byte but not 16-byte aligned
+    off2 = ctypes.c_void_p((1 << 21) + 2)        # not even 4-byte aligned
+    # a bf16 dispatch takes no scale buffer; FP8 scale words must be 4-byte aligned
+    assert lib.moe_dispatch(p, 128, Lp, 0, p, p, None, None) == INVALID
+    assert lib.moe_dispatch(p, 128, Lp, 1, p, off2, None, None) == INVALID
+    # tuning outside its ranges
+    for t in (ep.moe_tuning(stages=1), ep.moe_tuning(stages=9), ep.moe_tuning(chunk_bytes=100),
+              ep.moe_tuning(chunk_bytes=384), ep.moe_tuning(variant=4), ep.moe_tuning(num_channels=-1)):
+        assert lib.moe_dispatch(p, 128, Lp, 0, p, None, None, ctypes.byref(t)) == INVALID
+    assert lib.moe_combine(p, 64, Lp, p, p, None, ctypes.byref(ep.moe_tuning(variant=4))) == INVALID
+    # backward pair
+    assert lib.moe_dispatch_backward(p, 12, Lp, p, None, None) == INVALID              # hidden % 8
+    assert lib.moe_dispatch_backward(off4, 64, Lp, p, None, None) == INVALID           # misaligned rows
+    assert lib.moe_combine_backward(p, p, 64, Lp, p, p, None, None, None) == INVALID   # no grad_w
+    assert lib.moe_combine_backward(p, p, 64, Lp, off2, p, p, None, None) == INVALID   # misaligned weights
+    # low-latency layout
+    assert lib.moe_ll_dispatch(p, p, 16, 33, 8, 64, 4, p, p, p, p, None, None) == UNSUPPORTED    # K > 32
+    assert lib.moe_ll_dispatch(p, p, 1024, 8, 8, 64, 4, p, p, p, p, None, None) == UNSUPPORTED   # T*K > 4096
+    assert lib.moe_ll_dispatch(p, p, 16, 2, 8, 12, 4, p, p, p, p, None, None) == INVALID         # hidden % 8
+    assert lib.moe_ll_dispatch(p, p, 16, 2, 8, 64, 4, p, None, p, p, None, None) == INVALID      # no counts
+    assert lib.moe_ll_combine(p, p, p, 16, 2, 8, 64, 4, p, None, None, None) == INVALID          # no status
+    assert lib.moe_ll_combine(p, p, off2, 16, 2, 8, 64, 4, p, p, None, None) == INVALID         # misaligned w
+
+
 def test_status_strings(lib):
     from combine_moe_dispatch_02_gb300 import ep
     for s in range(7):
