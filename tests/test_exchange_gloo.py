@@ -142,12 +142,12 @@ def _run_ranks(target, port_base):
 
 
 def test_combine_matches_a_reverse_exchange_and_local_sum():
-    for rank, ok, n in _run_ranks(_combine_rank, 29900):
+    for rank, ok, n in _run_ranks(_combine_rank, 30300):
         assert ok is True, (rank, ok)
         assert n > 0
 
 
 def test_multi_source_layout_matches_an_all_to_all_exchange():
-    for rank, ok, n in _run_ranks(_rank, 29700):
+    for rank, ok, n in _run_ranks(_rank, 30100):
         assert ok is True, (rank, ok)
         assert n > 0
