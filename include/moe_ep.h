@@ -178,8 +178,12 @@ moe_status moe_layout_init_sources(moe_layout* L, int32_t S, int32_t source_toke
                                    int32_t R, void* device_mem, size_t bytes);
 
 /* Dispatch layout: counts, prefix offsets and token<->slot maps (all fields
- * above) from topk_idx int32 [T,K] (-1 = masked) and topk_w fp32 [T,K]
- * (may be NULL: expert_weight is then zero-filled).  Two kernels: a
+ * above), which size and address the worst-case-preallocated receive buffer
+ * (Hybrid-EP news article, "Availability and Integration"; the token-to-rank
+ * routing of "Inside the Nebius + PyTorch DeepSeek V3 recipe", "Mixture-of-
+ * experts and wide expert parallelism").  Inputs: topk_idx int32 [T,K]
+ * (-1 = masked) and topk_w fp32 [T,K] (may be NULL: expert_weight is then
+ * zero-filled).  Two kernels: a
  * warp-aggregated per-tile histogram with a decoupled-lookback scan over
  * E-wide count vectors (tiles claim ids from a ticket so every wait is on a
  * running CTA; every wait is bounded), then a finalize pass.
@@ -249,15 +253,21 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, const float* top
  *     q = E4M3(x * 2^-se), round to nearest even, saturating at 448.
  * x is bf16 [T, hidden]; hidden % 8 == 0 (hidden % 128 == 0 for both FP8
  * formats); x, recv_x 16-byte aligned, recv_scales 4-byte aligned.  Rows
- * past rank_offset[R] are not written.  Each CTA is an independent channel
- * over a contiguous chunk of tokens: TMA bulk loads of the row into shared
- * memory, then one TMA bulk store per destination row; no grid-wide
- * synchronisation (Hybrid-EP news article, "Technical Structure": each CUDA
- * block an independent channel). */
+ * past rank_offset[R] are not written.  bf16 (default kernel): each CTA is an
+ * independent channel over a contiguous range of (token, column chunk)
+ * items: TMA bulk loads of the chunk into shared memory, then one TMA bulk
+ * store per destination row; no grid-wide synchronisation (Hybrid-EP news
+ * article, "Technical Structure": each CUDA block an independent channel).
+ * FP8 and MXFP8 (default kernel): warps quantise 512-column segments in
+ * registers and store 16 codes per lane to every destination row. */
 moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
                         void* recv_x, void* recv_scales, void* stream, const moe_tuning* tuning);
 
-/* Combine: out[t,:] = bf16_rne( sum over k = 0..K-1 with expert_slot[t,k] >= 0
+/* Combine: the expert outputs back to each token's position, weighted by the
+ * router ("Inside the Nebius + PyTorch DeepSeek V3 recipe", "Mixture-of-
+ * experts and wide expert parallelism"; Hybrid-EP news article, "Technical
+ * Structure"):
+ * out[t,:] = bf16_rne( sum over k = 0..K-1 with expert_slot[t,k] >= 0
  * of topk_w[t,k] * y[expert_slot[t,k], :] ), accumulated in fp32 as a fused
  * multiply-add chain starting from 0 in ascending k.  y is bf16 [T*K, hidden]
  * in expert-major row order (row expert_offset[e] + j is expert e's j-th
