@@ -189,7 +189,7 @@ moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, 
     if (tuning && (tuning->num_channels < 0 || tuning->stages < 0 || tuning->stages > 8 ||
                    (tuning->stages != 0 && tuning->stages < 2) || tuning->chunk_bytes < 0 ||
                    (tuning->chunk_bytes != 0 && (tuning->chunk_bytes < 256 || tuning->chunk_bytes % 256 != 0)) ||
-                   tuning->variant < 0 || tuning->variant > 3))
+                   tuning->variant < 0 || tuning->variant > 4))
         return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_dispatch(x, hidden, L, format, recv_x, recv_scales,
                                           static_cast<cudaStream_t>(stream), tuning ? tuning->num_channels : 0,
@@ -202,7 +202,7 @@ moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, c
     if (!L || !L->status || hidden <= 0 || hidden % 8 != 0) return MOE_ERR_INVALID_ARG;
     if (L->T > 0 && (!y || !topk_w || !out)) return MOE_ERR_INVALID_ARG;
     if (!aligned16(y) || !aligned16(out) || (reinterpret_cast<uintptr_t>(topk_w) & 3u) != 0) return MOE_ERR_INVALID_ARG;
-    if (tuning && (tuning->num_channels < 0 || tuning->variant < 0 || tuning->variant > 3)) return MOE_ERR_INVALID_ARG;
+    if (tuning && (tuning->num_channels < 0 || tuning->variant < 0 || tuning->variant > 4)) return MOE_ERR_INVALID_ARG;
     return from_cuda(moe::launch_combine(y, hidden, L, topk_w, out, static_cast<cudaStream_t>(stream),
                                          tuning ? tuning->num_channels : 0, tuning ? tuning->variant : 0,
                                          timeout_of(tuning)));

@@ -254,6 +254,9 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
                             void* recv_x, void* recv_scales, cudaStream_t stream,
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
                             uint64_t timeout_ns);
+bool dispatch_wide_supported(const void* x, int32_t hidden, int32_t format, const void* recv_x);
+cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format, void* recv_x,
+                                 void* recv_scales, cudaStream_t stream, int32_t num_channels);
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
                            uint64_t timeout_ns);

@@ -71,12 +71,15 @@ typedef struct moe_tuning {
     int32_t  chunk_bytes;      /* dispatch: bf16 bytes of a row per pipeline item (a multiple of
                                   256, >= 256); 0 = 16384, i.e. whole rows up to hidden 8192     */
     int32_t  variant;          /* dispatch / combine kernel: 0 = default (bf16 dispatch: 1;
-                                  FP8 / MXFP8 dispatch: 2; combine: 16-byte vector loads with
+                                  FP8 / MXFP8 dispatch: 4; combine: 16-byte vector loads with
                                   the fma chain in registers), 1 = TMA bulk copies staged in
                                   shared memory (combine: K <= 8), 2 = 16-byte vector loads /
                                   stores (combine: as 0), 3 = FP8 / MXFP8 dispatch with
                                   warp-specialised roles (one TMA warp, eight quantiser warps;
-                                  bf16 dispatch and combine treat 3 as 0)                       */
+                                  bf16 dispatch and combine treat 3 as 0), 4 = dispatch with
+                                  32-byte vector loads / stores, a lane per 32 columns (needs
+                                  x and recv_x 32-byte aligned and, for bf16, hidden % 16 == 0;
+                                  otherwise it runs as 2; combine treats 4 as 0)                  */
     uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                   */
     uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                          */
     uint32_t reserved2;
@@ -129,7 +132,10 @@ typedef struct moe_layout {
 } moe_layout;
 
 /* Bytes of device memory moe_layout_init needs for these sizes (outputs +
- * scan workspace, each array 256-byte aligned).  0 if the sizes are invalid. */
+ * scan workspace, each array 256-byte aligned).  0 if the sizes are invalid.
+ * This is the layout's workspace-size query; it takes the capacity as well
+ * as T, K, E and R because one of the outputs it sizes, recv_src_token, has
+ * one entry per receive row. */
 size_t moe_layout_bytes(int32_t T, int32_t K, int32_t E, int32_t R, int64_t capacity);
 
 /* Carve the layout's arrays out of caller memory.  Host only: no CUDA call.
@@ -323,6 +329,9 @@ moe_status moe_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, cons
 moe_status moe_combine_backward(const uint16_t* grad_out, const uint16_t* y, int32_t hidden, const moe_layout* L,
                                 const float* topk_w, uint16_t* grad_y, float* grad_w, void* stream,
                                 const moe_tuning* tuning);
+
+/* Helpers of this library (the pages define no error interface; these two
+ * only read back and name the status of the calls above). */
 
 /* Synchronise `stream`, read the device status word, and map it to a status
  * (timeout first -- a timed-out scan also makes later kernels see slots out

@@ -5,7 +5,11 @@
 //   quotient:   moe::div_by_scale(x, s, r) vs __fdiv_rn(x, s) for every bf16
 //               x with |x| <= amax, bit for bit where |x| >= 2^-100 and
 //               |x/s| >= 2^-100 (the claimed exact range),
-//   codes:      their E4M3 codes, everywhere.
+//   codes:      their E4M3 codes, everywhere;
+//   magnitude:  moe::div_mag_by_scale(|x|, s, r) vs __fdiv_rn(|x|, s) under
+//               the same exactness condition, and the E4M3 code of that
+//               quotient with the sign bit of x OR'ed in vs the code of
+//               __fdiv_rn(x, s), everywhere.
 // The first few quotient and code mismatches are recorded.  Every index is
 // bounded by the array sizes.
 #include <cstdint>
@@ -53,6 +57,11 @@ __global__ void div_check_kernel(const uint16_t* amax_bits, int n_amax, unsigned
         const uint32_t c_ieee = moe::e4m3x2(q_ieee, 0.0f) & 0xffu;
         if (c_fast != c_ieee)
             record(&counters[1], examples + 4 * max_examples, max_examples, amax_bits[a_idx], xb, c_fast, c_ieee);
+        const float m = fabsf(x);
+        const float qm_fast = moe::div_mag_by_scale(m, s, r);
+        if (in_range && __float_as_uint(qm_fast) != __float_as_uint(__fdiv_rn(m, s))) atomicAdd(&counters[5], 1ull);
+        const uint32_t cm = (moe::e4m3x2(qm_fast, 0.0f) & 0xffu) | ((xb >> 8) & 0x80u);
+        if (cm != c_ieee) atomicAdd(&counters[6], 1ull);
     }
     const unsigned warp_n = __reduce_add_sync(0xffffffffu, local_n);
     if ((threadIdx.x & 31) == 0) atomicAdd(&counters[2], static_cast<unsigned long long>(warp_n));
@@ -61,7 +70,7 @@ __global__ void div_check_kernel(const uint16_t* amax_bits, int n_amax, unsigned
 }  // namespace
 
 // counters: [quotient mismatches, code mismatches, pairs checked, scale mismatches,
-//            reciprocal mismatches];
+//            reciprocal mismatches, magnitude-quotient mismatches, sign-OR code mismatches];
 // examples: 2 * max_examples records of 4 words.
 extern "C" int fp8_div_check(const uint16_t* amax_bits, int n_amax, unsigned long long* counters,
                              uint32_t* examples, int max_examples) {

@@ -95,9 +95,9 @@ def test_more_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.moe_dispatch(p, 128, Lp, 1, p, off2, None, None) == INVALID
     # tuning outside its ranges
     for t in (ep.moe_tuning(stages=1), ep.moe_tuning(stages=9), ep.moe_tuning(chunk_bytes=100),
-              ep.moe_tuning(chunk_bytes=384), ep.moe_tuning(variant=4), ep.moe_tuning(num_channels=-1)):
+              ep.moe_tuning(chunk_bytes=384), ep.moe_tuning(variant=5), ep.moe_tuning(num_channels=-1)):
         assert lib.moe_dispatch(p, 128, Lp, 0, p, None, None, ctypes.byref(t)) == INVALID
-    assert lib.moe_combine(p, 64, Lp, p, p, None, ctypes.byref(ep.moe_tuning(variant=4))) == INVALID
+    assert lib.moe_combine(p, 64, Lp, p, p, None, ctypes.byref(ep.moe_tuning(variant=5))) == INVALID
     # backward pair
     assert lib.moe_dispatch_backward(p, 12, Lp, p, None, None) == INVALID              # hidden % 8
     assert lib.moe_dispatch_backward(off4, 64, Lp, p, None, None) == INVALID           # misaligned rows

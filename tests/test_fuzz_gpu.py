@@ -38,7 +38,7 @@ def _cases(n=40, seed=20261202):
         T = rng.choice([1, 2, 17, 255, 256, 257, 1000, 2049, 3000])
         mask = rng.choice([0.0, 0.0, 0.1, 0.5, 1.0])
         dups = rng.random() < 0.3 or K > E
-        variant = rng.choice([0, 1, 2, 3])
+        variant = rng.choice([0, 1, 2, 3, 4])
         out.append((i, T, H, E, R, K, mask, dups, fmt, variant))
     return out
 

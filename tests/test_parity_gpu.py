@@ -28,7 +28,7 @@ def test_workload_parity_full_size(name):
     inp = make_inputs(wl)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8)
     assert o["status"] == 0
-    for variant in (0, 1, 2, 3):
+    for variant in (0, 1, 2, 3, 4):
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, fp8=wl.fp8, variant=variant)
         assert g["status"] == 0
         assert_parity(g, o, fp8=wl.fp8)
@@ -50,8 +50,10 @@ def test_workload_parity_full_size(name):
     (2500, 128, 256, 32, 8, 0.0, False, False, 10),  # many tiles, wide ranks
     (4096, 64, 1024, 256, 32, 0.0, False, False, 11),  # the documented maxima of E, R and K
     (700, 256, 128, 64, 8, 0.1, False, True, 12),   # FP8 with more than 32 destination ranks
+    (300, 48, 16, 4, 4, 0.0, False, False, 13),      # bf16 rows ending half-way through a 32-column lane
+    (257, 3200, 16, 8, 4, 0.05, False, True, 14),    # FP8 rows ending inside a 1024-column segment
 ])
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed, variant):
     idx = random_routing(T, K, E, seed, mask_frac=mask, allow_duplicates=dups)
     w = random_weights(T, K, seed)
@@ -121,7 +123,7 @@ def test_fp8_special_blocks():
     x[5, 256:384] = torch.tensor([1e-38] * 127 + [1.0])
     x = x.to(torch.bfloat16)
     o = oracle_run(x, idx, None, None, E, R, fp8=True)
-    for variant in (1, 2, 3):
+    for variant in (0, 1, 2, 3, 4):
         g = gpu_run(x, idx, None, None, E, R, fp8=True, variant=variant)
         assert_parity(g, o, fp8=True)
 
@@ -168,7 +170,7 @@ def test_tuning_variants_agree():
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R)
     for ch, st, cb, var in [(1, 2, 0, 1), (4, 3, 2048, 1), (16, 8, 4096, 1), (1000, 0, 0, 1), (100000, 0, 2048, 1),
                             (1, 0, 0, 2), (5, 0, 0, 2), (3000, 0, 0, 2), (0, 4, 0, 2), (7, 4, 0, 2), (0, 8, 0, 2),
-                            (5, 2, 0, 2)]:
+                            (5, 2, 0, 2), (1, 0, 0, 4), (7, 0, 0, 4), (100000, 0, 0, 4)]:
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, inp.y, wl.E, wl.R, num_channels=ch, stages=st,
                     chunk_bytes=cb, variant=var)
         assert_parity(g, o)
@@ -176,7 +178,8 @@ def test_tuning_variants_agree():
     for ch, st, cb, var in [(1, 2, 0, 1), (7, 4, 2048, 1), (3, 0, 0, 2), (999, 0, 0, 2),
                             (1, 0, 0, 3), (7, 0, 2048, 3), (999, 0, 4096, 3), (0, 4, 0, 2), (9, 4, 0, 2),
                             (0, 8, 0, 2), (3, 2, 0, 2),
-                            (100000, 0, 0, 1), (100000, 0, 2048, 1)]:     # one item per channel: one stage
+                            (100000, 0, 0, 1), (100000, 0, 2048, 1),     # one item per channel: one stage
+                            (1, 0, 0, 4), (7, 0, 0, 4), (100000, 0, 0, 4), (5, 0, 0, 0)]:
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=True, num_channels=ch, stages=st,
                     chunk_bytes=cb, variant=var)
         assert_parity(g, o8, fp8=True)
@@ -198,14 +201,14 @@ def test_mxfp8_parity_full_size(name):
     wl = WORKLOADS[name]
     inp = make_inputs(wl, with_y=False)
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=2)
-    for variant in (1, 2, 3):
+    for variant in (0, 1, 2, 3, 4):
         g = gpu_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=2, variant=variant)
         assert g["status"] == 0
         assert_parity(g, o, fp8=True)
 
 
 @pytest.mark.parametrize("T,H,E,R,K,seed", [(1, 128, 4, 2, 2, 0), (333, 384, 32, 8, 6, 1), (128, 9216, 16, 4, 4, 2)])
-@pytest.mark.parametrize("variant", [1, 2, 3])
+@pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_mxfp8_edge_cases(T, H, E, R, K, seed, variant):
     idx = random_routing(T, K, E, seed, mask_frac=0.1)
     g_ = torch.Generator().manual_seed(seed + 5)
@@ -220,3 +223,37 @@ def test_mxfp8_edge_cases(T, H, E, R, K, seed, variant):
     o = oracle_run(x, idx, None, None, E, R, fp8=2)
     assert g["status"] == 0
     assert_parity(g, o, fp8=True)
+
+
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_wide_dispatch_falls_back_when_only_16_byte_aligned(fmt):
+    """The 32-byte vector dispatch (the FP8 / MXFP8 default, variant 4) needs
+    32-byte aligned rows; x and the receive buffer at a 16-byte offset take
+    the 16-byte kernel instead, with the same results."""
+    from combine_moe_dispatch_02_gb300 import ep
+    T, H, E, R, K = 300, 1024, 32, 8, 6
+    idx = random_routing(T, K, E, 31, mask_frac=0.05)
+    g_ = torch.Generator().manual_seed(32)
+    x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
+    o = oracle_run(x, idx, None, None, E, R, fp8=fmt)
+    L = ep.Layout(T, K, E, R)
+    ep.moe_dispatch_layout(idx.cuda(), None, E, R, L)
+    xbuf = torch.empty(T * H + 8, dtype=torch.bfloat16, device="cuda")
+    x_off = xbuf[8:].view(T, H)                                  # 16 bytes past a 256-byte boundary
+    x_off.copy_(x.cuda())
+    assert x_off.data_ptr() % 32 == 16
+    esz = 2 if fmt == 0 else 1
+    rbuf = torch.empty(L.capacity * H * esz + 16, dtype=torch.uint8, device="cuda")
+    recv = rbuf[16:].view(torch.bfloat16).view(L.capacity, H) if fmt == 0 else rbuf[16:].view(L.capacity, H)
+    assert recv.data_ptr() % 32 == 16
+    scales = None if fmt == 0 else ep.alloc_recv(L, H, fmt)[1]
+    for variant in (0, 4):
+        ep.moe_dispatch(x_off, L, fmt, recv, scales, variant=variant)
+        assert ep.moe_layout_read_status(L) == (0, 0)
+        n = o["n_pairs"]
+        if fmt == 0:
+            assert np.array_equal(recv[:n].cpu().view(torch.int16).numpy().view(np.uint16), o["recv_x"])
+        else:
+            assert np.array_equal(recv[:n].cpu().numpy(), o["recv_q"])
+            assert np.array_equal(np.ascontiguousarray(scales[:n].cpu().numpy()).view(np.uint8),
+                                  np.ascontiguousarray(o["recv_scales"]).view(np.uint8))
