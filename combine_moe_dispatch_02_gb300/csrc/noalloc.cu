@@ -19,24 +19,74 @@ static __device__ __align__(256) unsigned char g_layout_scratch[MOE_NOALLOC_SCRA
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_addr[kMaxDevices] = {};
 
-// Device address of g_layout_scratch on the current device, looked up once
-// per device (with that device current) and cached.
+// The array's device address belongs to the context the library's module was
+// loaded into.  A cudaDeviceReset (or any teardown of the primary context)
+// and the context the runtime creates afterwards load the module again, at an
+// address that may differ, so each cached address is keyed by the identity of
+// the context it was looked up in.
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void* addr;
+};
+ScratchEntry g_scratch[kMaxDevices] = {};
+
+// Driver calls reached through the runtime (no link against libcuda).
+using CtxGetCurrentFn = int (*)(void**);
+using CtxGetIdFn = int (*)(void*, unsigned long long*);
+CtxGetCurrentFn g_ctx_get_current = nullptr;
+CtxGetIdFn g_ctx_get_id = nullptr;
+
+cudaError_t driver_entry_points() {
+    if (g_ctx_get_current && g_ctx_get_id) return cudaSuccess;
+    void* a = nullptr;
+    void* b = nullptr;
+    cudaDriverEntryPointQueryResult qa, qb;
+    cudaError_t err = cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &a, 12000, cudaEnableDefault, &qa);
+    if (err != cudaSuccess || qa != cudaDriverEntryPointSuccess || !a) return cudaErrorSymbolNotFound;
+    err = cudaGetDriverEntryPointByVersion("cuCtxGetId", &b, 12000, cudaEnableDefault, &qb);
+    if (err != cudaSuccess || qb != cudaDriverEntryPointSuccess || !b) return cudaErrorSymbolNotFound;
+    g_ctx_get_current = reinterpret_cast<CtxGetCurrentFn>(a);
+    g_ctx_get_id = reinterpret_cast<CtxGetIdFn>(b);
+    return cudaSuccess;
+}
+
+// Identity of the current context (0 if none is current yet).
+cudaError_t current_ctx_id(unsigned long long* id) {
+    void* ctx = nullptr;
+    *id = 0;
+    if (g_ctx_get_current(&ctx) != 0) return cudaErrorDeviceUninitialized;
+    if (ctx == nullptr) return cudaSuccess;
+    return g_ctx_get_id(ctx, id) == 0 ? cudaSuccess : cudaErrorDeviceUninitialized;
+}
+
+// Device address of g_layout_scratch in the current device's context: looked
+// up with cudaGetSymbolAddress once per device (with that device current),
+// and again whenever the context has been replaced since.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
+    err = driver_entry_points();
+    if (err != cudaSuccess) return err;
+    unsigned long long id = 0;
+    err = current_ctx_id(&id);
+    if (err != cudaSuccess) return err;
+    ScratchEntry& e = g_scratch[dev];
+    if (id == 0 || e.addr == nullptr || e.ctx_id != id) {
         void* p = nullptr;
-        err = cudaGetSymbolAddress(&p, g_layout_scratch);
+        err = cudaGetSymbolAddress(&p, g_layout_scratch);   // makes the device's context current if needed
         if (err != cudaSuccess) return err;
         if (p == nullptr) return cudaErrorInvalidSymbol;
-        g_scratch_addr[dev] = p;
+        err = current_ctx_id(&id);
+        if (err != cudaSuccess) return err;
+        if (id == 0) return cudaErrorDeviceUninitialized;
+        e.ctx_id = id;
+        e.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = e.addr;
     return cudaSuccess;
 }
 

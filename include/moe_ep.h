@@ -227,8 +227,10 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w,
  * each call clears the parts that must start at zero.  Calls that overlap on
  * the GPU (on different streams without ordering, or from several threads)
  * race on it.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it: make that
- * first call before any stream capture.  No cudaMalloc, cudaFree or other
+ * (cudaGetSymbolAddress, with that device current) and caches it, keyed by the
+ * device's current context: make that first call before any stream capture.
+ * After a cudaDeviceReset the next call looks the address up again in the new
+ * context (also before any capture).  No cudaMalloc, cudaFree or other
  * allocating routine is called. */
 #define MOE_NOALLOC_SCRATCH_BYTES (8u << 20)
 

@@ -109,3 +109,38 @@ def test_noalloc_layout_rejects_sizes_beyond_its_scratch(ep):
     st = ep.lib().moe_dispatch_layout_noalloc(ctypes.c_void_p(dummy.data_ptr()), None, E, R, ctypes.byref(L),
                                               None, None)
     assert st == ep.MOE_ERR_UNSUPPORTED
+
+
+def test_noalloc_call_after_a_timed_out_one_on_another_stream(ep):
+    """The shared array after a call whose scan waits ran out (a test hook
+    makes the first tile never publish; 20 ms bound): a later call, on a
+    second stream ordered after the first by an event, starts clean and
+    matches the regular entry point bit for bit."""
+    wl = WORKLOADS["dsv3"]
+    T = 2048                                               # 32 scan tiles
+    inp = make_inputs(wl.scaled(T), with_y=False)
+    idx, w = inp.topk_idx.cuda(), inp.topk_w.cuda()
+    want, st = _regular(ep, idx, w, wl.E, wl.R)
+    assert st == (0, 0)
+    L, out = _caller_owned_layout(ep, T, wl.K, wl.E, wl.R)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    s1.wait_stream(torch.cuda.current_stream())
+    ep.moe_dispatch_layout_noalloc(idx, w, wl.E, wl.R, L, stream=s1, wait_timeout_ns=20_000_000,
+                                   debug_flags=ep.MOE_DEBUG_STALL_FIRST_TILE)
+    done = torch.cuda.Event()
+    done.record(s1)
+    s2.wait_event(done)
+    ep.moe_dispatch_layout_noalloc(idx, w, wl.E, wl.R, L, stream=s2)
+    s2.synchronize()
+    assert int(out["status"].item()) == 0
+    for f in FIELDS:
+        got = out[f].cpu().numpy()
+        if f == "expert_weight":
+            assert np.array_equal(got.view(np.uint32), want[f].view(np.uint32)), f
+        else:
+            assert np.array_equal(got, want[f]), f
+    # and the timed-out call itself reported the timeout
+    ep.moe_dispatch_layout_noalloc(idx, w, wl.E, wl.R, L, stream=s1, wait_timeout_ns=20_000_000,
+                                   debug_flags=ep.MOE_DEBUG_STALL_FIRST_TILE)
+    s1.synchronize()
+    assert int(out["status"].item()) & ep.MOE_DEVERR_TIMEOUT
