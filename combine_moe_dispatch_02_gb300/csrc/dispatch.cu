@@ -20,13 +20,14 @@
 //   * FP8 (TMA variant): the CTA's warps compute block amax, scale and E4M3
 //     codes into an output stage, which TMA bulk stores send to every
 //     destination row; the scales go out with plain stores.
-// FP8 and MXFP8 default to the 32-byte vector kernel of dispatch_wide.cu (no
-// staging: each warp quantises 1024-column segments in registers and stores
-// the codes straight to every destination row), which measured fastest for
-// them on GB300; the 16-byte vector kernel further down (variant 2) serves
-// where the pointers are only 16-byte aligned.  bf16 defaults to the TMA
-// kernel.  A warp-specialised TMA variant (one copy warp, eight quantiser
-// warps) is kept as variant 3.
+// All three formats default to the 32-byte vector kernel of dispatch_wide.cu
+// (no staging: each warp moves -- and for FP8 / MXFP8 quantises -- one
+// 1024-column segment in registers and stores it straight to every
+// destination row), which measured fastest for every format and shape on
+// GB300.  Where the pointers are only 16-byte aligned, bf16 takes the TMA
+// kernel below (variant 1) and FP8 / MXFP8 the 16-byte vector kernel
+// (variant 2).  A warp-specialised TMA variant (one copy warp, eight
+// quantiser warps) is kept as variant 3.
 // x is read from HBM once; the receive rows are written once each.
 #include <climits>
 
@@ -636,13 +637,14 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
                             uint64_t timeout_ns) {
     if (L->T == 0) return cudaSuccess;
-    // FP8 / MXFP8 default and variant 4: the 32-byte vector kernel
-    // (dispatch_wide.cu); the 16-byte one (variant 2) where the pointers or
-    // the row pitch do not keep 32-byte alignment
-    if (variant == 4 || (variant == 0 && format != MOE_FORMAT_BF16)) {
+    // The default and variant 4: the 32-byte vector kernel (dispatch_wide.cu);
+    // where the pointers or the row pitch do not keep 32-byte alignment, the
+    // 16-byte kernels: TMA staging for bf16 (variant 1), the 16-byte vector
+    // kernel for FP8 / MXFP8 (variant 2)
+    if (variant == 4 || variant == 0) {
         if (dispatch_wide_supported(x, hidden, format, recv_x))
             return launch_dispatch_wide(x, hidden, L, format, recv_x, recv_scales, stream, num_channels);
-        variant = 2;
+        variant = format == MOE_FORMAT_BF16 ? 1 : 2;
     }
     DispatchArgs a;
     a.x = reinterpret_cast<const uint8_t*>(x);

@@ -18,10 +18,12 @@
 //     the segment (32 bytes) leave in one more store instruction;
 //   * bf16 (no quantisation): the lane's 64 bytes leave in two 32-byte
 //     stores per destination row;
-//   * each warp takes a contiguous run of items (token-major), so the token /
-//     segment indices advance by increments (no per-item division) and the
-//     destination list of a token (its recv_slot row, one ballot) is reused
-//     by all of the token's segments the warp holds;
+//   * by default every warp takes one item (many short-lived CTAs, which the
+//     block scheduler balances); with fewer channels (moe_tuning) each warp
+//     takes a contiguous run of items (token-major), whose token / segment
+//     indices advance by increments (no per-item division) and whose
+//     destination list (the recv_slot row, one ballot) is reused by all of a
+//     token's segments the warp holds;
 //   * the next item's loads are issued once the current item is quantised,
 //     before its stores.
 //
@@ -48,7 +50,6 @@ constexpr int kWideThreads = 256;
 constexpr int kWideWarps = kWideThreads / 32;
 constexpr int kWideSeg = 1024;          // columns per item
 constexpr int kWideLaneCols = 32;       // columns per lane
-constexpr int kWideWaves = 4;           // default grid: waves of resident CTAs
 
 struct WideArgs {
     const uint8_t* x;            // bf16 [T, H]
@@ -230,51 +231,67 @@ __device__ __forceinline__ void wide_emit(const WideArgs& a, int32_t t, int32_t 
 }
 
 // FMT 0: bf16 rows; 1: FP8 with fp32 1x128 scales; 2: MXFP8 (E8M0 1x32
-// scales).  Registers bounded to four CTAs of 256 threads per SM (FP8: 64
-// registers, 12 bytes of spill; unbounded it takes 77 and three CTAs, which
-// measured the same).  One item in registers per warp: the next item's loads are issued as soon as
-// the current one is quantised (bf16: once it is stored), before its stores,
-// so the load latency overlaps the stores and the other warps' work.  (Two
-// items in registers per warp measured slower on GB300 at every shape: the
-// registers it needs cost occupancy or spill.)
-template <int FMT>
+// scales).  ONE: the default grid, exactly one item per warp (warp w takes
+// item w), straight-line code whose registers (FP8 63, MXFP8 48, bf16 39)
+// let four, five and six CTAs of 256 threads share an SM.  Otherwise each
+// warp takes a contiguous run of items with one item in registers: the next
+// item's loads are issued as soon as the current one is quantised (bf16: once
+// it is stored), before its stores, so the load latency overlaps the stores
+// and the other warps' work; registers bounded to four CTAs per SM (FP8: 64
+// registers and 12 bytes of spill).  Two items in registers per warp measured
+// slower on GB300 at every shape: the registers they need cost occupancy or
+// spill.
+template <int FMT, bool ONE>
 __global__ void __launch_bounds__(kWideThreads, 4)
 dispatch_wide_kernel(WideArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * kWideWarps + (threadIdx.x >> 5);
-    const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kWideWarps;
-    const int64_t i0 = a.n_items * warp_id / n_warps;
-    const int64_t i1 = a.n_items * (warp_id + 1) / n_warps;
     bool bad = false;
-    if (i0 < i1) {
-        int n = static_cast<int>(i1 - i0);
-        int32_t t = static_cast<int32_t>(i0 / a.nseg);
-        int32_t seg = static_cast<int32_t>(i0 - static_cast<int64_t>(t) * a.nseg);
-        uint32_t codes[8];
-        WideItem it;
-        wide_load(it, a, t, seg, lane, -1, -1);
-        while (true) {
-            const int32_t ct = it.t, cseg = it.seg, cslot = it.slot;
-            if constexpr (FMT == 0) {
-                wide_emit<FMT>(a, ct, cseg, cslot, it.w, codes, 0u, lane, bad);
-                if (--n == 0) break;
-                if (++seg == a.nseg) { seg = 0; ++t; }
-                wide_load(it, a, t, seg, lane, ct, cslot);
-            } else {
-                const uint32_t sw = wide_quant<FMT>(it, codes);
-                const bool more = n > 1;
-                if (more) {
+    if constexpr (ONE) {
+        if (warp_id < a.n_items) {
+            const int32_t t = static_cast<int32_t>(warp_id / a.nseg);
+            const int32_t seg = static_cast<int32_t>(warp_id - static_cast<int64_t>(t) * a.nseg);
+            uint32_t codes[8];
+            WideItem it;
+            wide_load(it, a, t, seg, lane, -1, -1);
+            const uint32_t sw = wide_quant<FMT>(it, codes);
+            wide_emit<FMT>(a, t, seg, it.slot, it.w, codes, sw, lane, bad);
+        }
+    } else {
+        const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kWideWarps;
+        const int64_t i0 = a.n_items * warp_id / n_warps;
+        const int64_t i1 = a.n_items * (warp_id + 1) / n_warps;
+        if (i0 < i1) {
+            int n = static_cast<int>(i1 - i0);
+            int32_t t = static_cast<int32_t>(i0 / a.nseg);
+            int32_t seg = static_cast<int32_t>(i0 - static_cast<int64_t>(t) * a.nseg);
+            uint32_t codes[8];
+            WideItem it;
+            wide_load(it, a, t, seg, lane, -1, -1);
+            while (true) {
+                const int32_t ct = it.t, cseg = it.seg, cslot = it.slot;
+                if constexpr (FMT == 0) {
+                    wide_emit<FMT>(a, ct, cseg, cslot, it.w, codes, 0u, lane, bad);
+                    if (--n == 0) break;
                     if (++seg == a.nseg) { seg = 0; ++t; }
                     wide_load(it, a, t, seg, lane, ct, cslot);
+                } else {
+                    const uint32_t sw = wide_quant<FMT>(it, codes);
+                    const bool more = n > 1;
+                    if (more) {
+                        if (++seg == a.nseg) { seg = 0; ++t; }
+                        wide_load(it, a, t, seg, lane, ct, cslot);
+                    }
+                    wide_emit<FMT>(a, ct, cseg, cslot, nullptr, codes, sw, lane, bad);
+                    if (--n == 0) break;
                 }
-                wide_emit<FMT>(a, ct, cseg, cslot, nullptr, codes, sw, lane, bad);
-                if (--n == 0) break;
             }
         }
     }
     pdl_trigger();
-    if (__syncthreads_or(bad) && threadIdx.x == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
+    // per warp, no CTA-wide barrier: a warp that is done leaves at once
+    if (__any_sync(0xffffffffu, bad) && lane == 0) atomicOr(a.status, MOE_DEVERR_CAPACITY);
 }
 
 }  // namespace
@@ -297,28 +314,30 @@ cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_la
     a.nseg = (hidden + kWideSeg - 1) / kWideSeg;
     a.n_items = static_cast<int64_t>(L->T) * a.nseg;
     a.status = L->status;
-    const void* fn = format == MOE_FORMAT_MXFP8 ? reinterpret_cast<const void*>(dispatch_wide_kernel<2>)
-                     : format == MOE_FORMAT_FP8 ? reinterpret_cast<const void*>(dispatch_wide_kernel<1>)
-                                                : reinterpret_cast<const void*>(dispatch_wide_kernel<0>);
-    int per_sm = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kWideThreads, 0);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) per_sm = 1;
-    // Default grid: four waves of resident CTAs, each warp a contiguous run of
-    // about 1.5 items at the DeepSeek-V3 shape.  CTAs that finish early make
-    // room for the next wave, so the block scheduler balances the tokens'
-    // unequal destination counts; on GB300 this beat one persistent wave by
-    // 4 us at the DeepSeek-V3 shape and 4.5 us at the DeepSeek-16B-like shape
-    // (back-to-back launches), and lost 1 us at the Zipf-skewed Qwen-like one.
-    int64_t grid = num_channels > 0 ? num_channels : static_cast<int64_t>(sm_count()) * per_sm * kWideWaves;
-    const int64_t need = (a.n_items + kWideWarps - 1) / kWideWarps;     // at least one item per warp
+    // Default grid: one item per warp (the last CTA may hold fewer).  The
+    // block scheduler then balances the tokens' unequal destination counts
+    // CTA by CTA, and no warp of a CTA waits for a sibling with more items.
+    // On GB300 (back-to-back launches over buffers larger than L2) this beat
+    // four waves of CTAs holding about 1.5 items per warp by 1.2 us at the
+    // DeepSeek-V3 shape (FP8 35.1 -> 33.9 us) and 1.7 us at the DeepSeek-16B-
+    // like shape, and one persistent wave by 5-7 us; at the Zipf-skewed
+    // Qwen-like shape two items per warp were 1.4 us faster.  CTAs of one or
+    // two warps measured the same except where their sheer number (32,768
+    // one-warp CTAs in 24 us) outran the CTA launch rate.
+    const int64_t need = (a.n_items + kWideWarps - 1) / kWideWarps;     // one item per warp
+    int64_t grid = num_channels > 0 ? num_channels : need;
     if (grid > need) grid = need;
     if (grid < 1) grid = 1;
     if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     const dim3 g(static_cast<unsigned>(grid)), b(kWideThreads);
-    if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2>, g, b, 0, stream, a);
-    if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1>, g, b, 0, stream, a);
-    return launch_pdl(dispatch_wide_kernel<0>, g, b, 0, stream, a);
+    if (grid == need) {           // one item per warp
+        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, true>, g, b, 0, stream, a);
+        if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, true>, g, b, 0, stream, a);
+        return launch_pdl(dispatch_wide_kernel<0, true>, g, b, 0, stream, a);
+    }
+    if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, false>, g, b, 0, stream, a);
+    if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, false>, g, b, 0, stream, a);
+    return launch_pdl(dispatch_wide_kernel<0, false>, g, b, 0, stream, a);
 }
 
 }  // namespace moe

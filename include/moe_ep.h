@@ -63,23 +63,26 @@ typedef enum moe_status {
 /* Optional launch tuning; pass NULL for the defaults. */
 typedef struct moe_tuning {
     int32_t  num_channels;     /* CTAs ("independent channels") for dispatch / combine; 0 = auto
-                                  (bf16 dispatch: one (token, chunk) item per CTA; vector
-                                  dispatch and combine: four waves of resident CTAs)            */
+                                  (dispatch: one item per warp (32-byte kernel) or per CTA
+                                  (TMA kernel); 16-byte vector dispatch and combine: four waves
+                                  of resident CTAs)                                              */
     int32_t  stages;           /* dispatch pipeline depth per channel, 2..8; 0 = auto (TMA
                                   kernels: at most the items a channel holds; variant 2: 2 / 4 / 8
                                   = batches of 1 / 2 / 4 items, two batches in flight)          */
     int32_t  chunk_bytes;      /* dispatch: bf16 bytes of a row per pipeline item (a multiple of
                                   256, >= 256); 0 = 16384, i.e. whole rows up to hidden 8192     */
-    int32_t  variant;          /* dispatch / combine kernel: 0 = default (bf16 dispatch: 1;
-                                  FP8 / MXFP8 dispatch: 4; combine: 16-byte vector loads with
-                                  the fma chain in registers), 1 = TMA bulk copies staged in
+    int32_t  variant;          /* dispatch / combine kernel: 0 = default (dispatch: 4, or where
+                                  its alignment does not hold, 1 for bf16 and 2 for FP8 /
+                                  MXFP8; combine: 16-byte vector loads with the fma chain in
+                                  registers), 1 = TMA bulk copies staged in
                                   shared memory (combine: K <= 8), 2 = 16-byte vector loads /
                                   stores (combine: as 0), 3 = FP8 / MXFP8 dispatch with
                                   warp-specialised roles (one TMA warp, eight quantiser warps;
                                   bf16 dispatch and combine treat 3 as 0), 4 = dispatch with
                                   32-byte vector loads / stores, a lane per 32 columns (needs
                                   x and recv_x 32-byte aligned and, for bf16, hidden % 16 == 0;
-                                  otherwise it runs as 2; combine treats 4 as 0)                  */
+                                  otherwise it runs as 1 for bf16 and as 2 for FP8 / MXFP8;
+                                  combine treats 4 as 0)                                         */
     uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                   */
     uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                          */
     uint32_t reserved2;
