@@ -1,12 +1,13 @@
 #!/usr/bin/env python
 """Benchmark of the MoE dispatch / combine hot path on one GB300 (or N replicas).
 
-One step = dispatch layout (2 kernels) -> bf16 dispatch -> combine over the
+One step = dispatch layout (2 kernels) -> dispatch -> combine over the
 DeepSeek-V3-shaped workload: 4096 tokens, hidden 7168, 256 experts over 8
-virtual ranks, top-8 (seeded synthetic routing and activations).  Inputs are
-resident in HBM; L2 is flushed (a 256 MB write, then a 256 MB read of another
-buffer) between timed steps, outside the CUDA-event brackets.  Prints one
-JSON line.
+virtual ranks, top-8 (seeded synthetic routing and activations).  The
+dispatch writes bf16 rows, or FP8 E4M3 rows with 1x128 fp32 scales under
+``--workload dsv3_fp8``.  Inputs are resident in HBM; L2 is flushed (a 256 MB
+write, then a 256 MB read of another buffer) between timed steps, outside the
+CUDA-event brackets.  Prints one JSON line.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -33,18 +34,24 @@ sys.path.insert(0, ROOT)
 METRIC = "dispatch / combine HBM GB/s and tokens/s on 1 GB300, % of HBM roofline"
 WORKLOAD = "dsv3"
 L2_FLUSH_BYTES = 256 << 20
-
-
-# ------------------------------------------------------------ byte accounting
+# GB300 datasheet HBM3e bandwidth (~8 TB/s): the second denominator of every
+# fraction, next to the measured copy rate
+SPEC_HBM_GBS = 8000.0
+L2_POLICY = ("GPU arm: L2 flushed between timed repetitions (256 MB write, then 256 MB read of another "
+             "buffer), outside the event brackets; CPU oracle arm: host memory, no flush")
 
 # Secondary legs run after the timed step (each reported under "ops"); the
-# headline step and its layout / dispatch split always run.
-LEGS = ("fp8", "mxfp8", "backward", "ll", "sources", "workloads", "channels", "e2e")
-# the other routing shapes, measured as an eager flushed step each (secondary figures)
+# headline step and its per-operator split always run.
+LEGS = ("formats", "backward", "ll", "sources", "workloads", "channels", "e2e")
+# the other routing shapes, measured as steps of their own (secondary figures)
 OTHER_WORKLOADS = ("qwen_skew", "ds16_wide")
 # CTA counts of the channel sweep (the pages fill NVLink with 4 SMs; HBM needs many more)
 SWEEP_CTAS = (4, 8, 16, 32, 64, 152, 304, 608, 1216)
 
+FORMAT_NAMES = {0: "bf16", 1: "fp8", 2: "mxfp8"}
+
+
+# ------------------------------------------------------------ byte accounting
 
 def workload_label(wl):
     """What the workload is, with its sizes."""
@@ -68,6 +75,28 @@ def algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, capacity):
             "combine": combine}
 
 
+def dispatch_key(fmt: int) -> str:
+    """Key of algorithmic_bytes for a receive format."""
+    return {0: "dispatch", 1: "dispatch_fp8", 2: "dispatch_mxfp8"}[int(fmt)]
+
+
+def step_label(fmt: int) -> str:
+    return {0: "layout + bf16 dispatch + combine",
+            1: "layout + FP8 E4M3 dispatch (1x128 fp32 scales) + combine of bf16 expert outputs"}[int(fmt)]
+
+
+def step_config(wl, fmt, n_pairs, capacity, world, T_sample=None):
+    """The `config` object of both arms: the workload, the step and the L2
+    policy; a CPU sample of fewer tokens than the workload says so in its
+    workload string."""
+    label = workload_label(wl)
+    if T_sample is not None and T_sample < wl.T:
+        label += f" (first {T_sample} of {wl.T} tokens per step)"
+    return {"workload": label, "T": wl.T if T_sample is None else T_sample, "H": wl.H, "E": wl.E, "R": wl.R,
+            "K": wl.K, "n_pairs": n_pairs, "capacity": capacity, "step": step_label(fmt), "l2": L2_POLICY,
+            "parallelism": f"replicas x{world}"}
+
+
 def measured_peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -77,25 +106,20 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-def committed_traffic(kernel_file: str, profile_name: str):
-    """DRAM bytes per launch from a committed ncu summary, or None if the
-    summary is missing or the kernel source changed since it was taken."""
-    prof = os.path.join(ROOT, "profiles", profile_name)
-    src = os.path.join(ROOT, "combine_moe_dispatch_02_gb300", "csrc", kernel_file)
-    if not os.path.exists(prof):
-        return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-    vals = {}
-    for line in open(prof):
-        if ":" in line and line.strip().startswith("- "):
-            k, v = line.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_sha256_16") != sha:
-        return None
-    try:
-        return int(float(vals["dram_bytes_per_full_launch"]))
-    except (KeyError, ValueError):
-        return None
+def committed_traffic(record: str):
+    """DRAM bytes per launch from a committed one-launch ncu record
+    (profiles/<record>.json), with the capture it came from; (None, why) if
+    the record is missing or a source it names has changed since."""
+    path = os.path.join(ROOT, "profiles", record + ".json")
+    if not os.path.exists(path):
+        return None, "no committed capture"
+    with open(path) as f:
+        rec = json.load(f)
+    for src, sha in rec["source_sha256_16"].items():
+        with open(os.path.join(ROOT, "combine_moe_dispatch_02_gb300", "csrc", src), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != sha:
+                return None, f"{src} changed since the committed capture"
+    return int(rec["dram_bytes_per_launch"]), f"profiles/{record}.json: {rec['capture']}"
 
 
 # ------------------------------------------------------------- multi-rank
@@ -196,6 +220,84 @@ class L2Flush:
         self.b.max()
 
 
+# ------------------------------------------------------------------ timers
+
+class Timer:
+    """Flushed, warmed-up CUDA-event timing on one stream.
+
+    eager(body, n, marks): `warmup` untimed repetitions of body(mark), then n
+    recorded ones; body calls mark(i) for i = 0 .. marks-1 between its
+    launches; returns, per interval, the list of per-repetition times (ms).
+    graph(fn, n): fn(stream) captured once as a CUDA graph, then replayed the
+    same way with events only at its two ends; returns per-replay times (ms).
+    """
+
+    def __init__(self, torch, dev, stream, flush, warmup):
+        self.torch, self.dev, self.stream, self.flush, self.warmup = torch, dev, stream, flush, warmup
+
+    def _ev(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    def eager(self, body, n, marks):
+        for _ in range(self.warmup):
+            self.flush()
+            body(lambda i: None)
+        evs = []
+        for _ in range(n):
+            e = [self._ev() for _ in range(marks)]
+            self.flush()
+            body(lambda i, e=e: e[i].record(self.stream))
+            evs.append(e)
+        self.torch.cuda.synchronize(self.dev)
+        return [[e[i].elapsed_time(e[i + 1]) for e in evs] for i in range(marks - 1)]
+
+    def capture(self, fn):
+        torch = self.torch
+        g = torch.cuda.CUDAGraph()
+        cs = torch.cuda.Stream(self.dev)
+        cs.wait_stream(self.stream)
+        with torch.cuda.graph(g, stream=cs):
+            fn(cs)
+        self.stream.wait_stream(cs)
+        return g
+
+    def replay(self, g, n):
+        for _ in range(self.warmup):
+            self.flush()
+            g.replay()
+        evs = []
+        for _ in range(n):
+            e0, e1 = self._ev(), self._ev()
+            self.flush()
+            e0.record(self.stream)
+            g.replay()
+            e1.record(self.stream)
+            evs.append((e0, e1))
+        self.torch.cuda.synchronize(self.dev)
+        return [a.elapsed_time(b) for a, b in evs]
+
+    def graph(self, fn, n):
+        return self.replay(self.capture(fn), n)
+
+    def back_to_back(self, fns, n):
+        """fns (each fn(stream) one launch, typically on its own buffer set)
+        captured back to back in one graph, replayed like graph(); per-launch
+        times (ms): a replay's time over len(fns)."""
+        g = self.capture(lambda s: [f(s) for f in fns])
+        return [t / len(fns) for t in self.replay(g, n)]
+
+
+def pct(ms_list):
+    """p10 / p50 / p90 of per-repetition times, in us."""
+    q = statistics.quantiles(ms_list, n=10, method="inclusive") if len(ms_list) > 1 else [ms_list[0]] * 9
+    return {"p10": round(q[0] * 1e3, 2), "p50": round(statistics.median(ms_list) * 1e3, 2),
+            "p90": round(q[8] * 1e3, 2)}
+
+
+def gbps(nbytes, ms):
+    return nbytes / (ms * 1e-3) / 1e9
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -208,6 +310,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
     wl = WORKLOADS[args.workload]
+    fmt = ep.MOE_FORMAT_FP8 if wl.fp8 else ep.MOE_FORMAT_BF16
     inp = make_inputs(wl, seed=rank)
     T, H, E, R, K = wl.T, wl.H, wl.E, wl.R, wl.K
 
@@ -216,55 +319,81 @@ def run_ours(args, rank, world, local_rank):
     idx = inp.topk_idx.to(dev)
     w = inp.topk_w.to(dev)
     y = inp.y.to(dev)
-    recv, _ = ep.alloc_recv(L, H, False, device=dev)
+    recv, recv_s = ep.alloc_recv(L, H, fmt, device=dev)
     out = torch.empty(T, H, dtype=torch.bfloat16, device=dev)
     flush = L2Flush(dev)
     stream = torch.cuda.current_stream(dev)
+    tm = Timer(torch, dev, stream, flush, args.warmup)
+    peak, peak_kind = measured_peaks()
+    # repetitions of each secondary figure (each after its own warm-up)
+    n_sec = max(20, min(args.steps // 4, 400))
+    n_stream = max(10, n_sec // 8)
 
-    def step(evs=None, split=False):
-        if evs:
-            evs[0].record(stream)
-        ep.moe_dispatch_layout(idx, w, E, R, L, stream)
-        if split:
-            evs[1].record(stream)
-        ep.moe_dispatch(x, L, False, recv, None, stream)
-        if evs:
-            evs[2 if split else 1].record(stream)
-        ep.moe_combine(y, L, w, out, stream)
-        if evs:
-            evs[3 if split else 2].record(stream)
+    def check(layout, what):
+        st, flags = ep.moe_layout_read_status(layout, stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st} ({ep.moe_status_string(st)}) flags {flags:#x} {what}")
+
+    def step_ops(s, f=fmt, rq=recv, rs=recv_s):
+        ep.moe_dispatch_layout(idx, w, E, R, L, s)
+        ep.moe_dispatch(x, L, f, rq, rs, s)
+        ep.moe_combine(y, L, w, out, s)
 
     for _ in range(args.warmup):
         flush()
-        step()
+        step_ops(stream)
     torch.cuda.synchronize(dev)
-    st, flags = ep.moe_layout_read_status(L, stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st} ({ep.moe_status_string(st)}) flags {flags:#x}")
+    check(L, "after the warm-up steps")
     n_pairs = int(L.rank_offset[R].item())
     n_valid = int(L.expert_offset[E].item())
     ab = algorithmic_bytes(T, H, E, R, K, n_pairs, n_valid, L.capacity)
-    step_bytes = ab["layout"] + ab["dispatch"] + ab["combine"]
+    dkey = dispatch_key(fmt)
+    step_bytes = ab["layout"] + ab[dkey] + ab["combine"]
+
+    def hbm_op(nbytes, ms_list, eager_ms=None, stream_ms=None, **extra):
+        """Graph-replayed figure (the fraction's time) and, if given, the
+        eager one with events between launches and the back-to-back one over
+        rotating buffer sets (frac_stream)."""
+        ms = statistics.mean(ms_list)
+        d = {"us": round(ms * 1e3, 2), "us_pct": pct(ms_list), "bytes": nbytes, "GB/s": round(gbps(nbytes, ms), 1),
+             "frac": round(gbps(nbytes, ms) / peak, 4), "frac_spec": round(gbps(nbytes, ms) / SPEC_HBM_GBS, 4)}
+        if eager_ms is not None:
+            d["eager_us"] = round(statistics.mean(eager_ms) * 1e3, 2)
+        if stream_ms is not None:
+            sm = statistics.mean(stream_ms)
+            d["stream_us"] = round(sm * 1e3, 2)
+            d["frac_stream"] = round(gbps(nbytes, sm) / peak, 4)
+        d.update(extra)
+        return d
+
+    # back-to-back launches over NB rotating buffer sets: every launch's inputs
+    # were last touched NB launches earlier, with well over L2's 129 MB of
+    # other traffic in between, so none is served from L2, and the launches
+    # pay the write-back of their predecessors' dirty lines as a pipeline of
+    # layers would; no event or launch gap sits inside the figure
+    NB = 4
+    xs = [x] + [x.clone() for _ in range(NB - 1)]
+    ys = [y] + [y.clone() for _ in range(NB - 1)]
+    outs = [out] + [torch.empty_like(out) for _ in range(NB - 1)]
+
+    def rotating(op, bufs):
+        return [lambda s, i=i: op(s, bufs[i % NB], i % NB) for i in range(2 * NB)]
+
+    def stream_dispatch(f):
+        sets = [ep.alloc_recv(L, H, f, device=dev) for _ in range(NB)]
+        ms = tm.back_to_back(rotating(lambda s, b, i: ep.moe_dispatch(xs[i], L, f, b[0], b[1], s), sets), n_stream)
+        del sets
+        return ms
 
     # The timed steps replay the whole step as one CUDA graph, captured once (the
     # programmatic launch chain layout -> dispatch is kept as graph edges), with
     # events only at the step's two ends: an event between two kernels costs
     # ~2 us of GPU time and cuts the programmatic overlap.  Per-operator times
-    # come from a separate pass with events between the operators.
-    cap = torch.cuda.Stream(dev)
-    g_step = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_step, stream=cap):
-        ep.moe_dispatch_layout(idx, w, E, R, L, cap)
-        ep.moe_dispatch(x, L, False, recv, None, cap)
-        ep.moe_combine(y, L, w, out, cap)
+    # come from separate passes.
+    g_step = tm.capture(step_ops)
     for _ in range(3):
         flush()
         g_step.replay()
-
-    def graph_step(evs):
-        evs[0].record(stream)
-        g_step.replay()
-        evs[1].record(stream)
 
     events = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     sampler = ClockSampler(local_rank, args.clocks_log.replace("{rank}", str(rank)) if args.clocks_log else None)
@@ -276,100 +405,108 @@ def run_ours(args, rank, world, local_rank):
     t_wall0 = time.perf_counter()
     for s in range(args.steps):
         flush()                   # L2 flush, outside the event brackets
-        graph_step(events[s])
+        events[s][0].record(stream)
+        g_step.replay()
+        events[s][1].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
     t_wall = time.perf_counter() - t_wall0
     clocks = sampler.stop()
-    st, flags = ep.moe_layout_read_status(L, stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st} after timed steps")
-
+    check(L, "after the timed steps")
     tot = [e[0].elapsed_time(e[1]) for e in events]
-    ms_step = statistics.mean(tot)
-    # per-operator split: a separate eager pass of the same step with events
-    # between the operators (each after an L2 flush, like the timed steps)
-    n_split = max(args.steps // 4, 3)
-    ev_split = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(n_split)]
-    for e in ev_split:
-        flush()
-        step(e, split=True)
-    torch.cuda.synchronize(dev)
-    lay = [e[0].elapsed_time(e[1]) for e in ev_split]
-    dis = [e[1].elapsed_time(e[2]) for e in ev_split]
-    com = [e[2].elapsed_time(e[3]) for e in ev_split]
-    ms_step = max_over_ranks(ms_step, world, dev)
+    ms_step = max_over_ranks(statistics.mean(tot), world, dev)
 
-    peak, peak_kind = measured_peaks()
-    gbps = lambda b, ms: b / (ms * 1e-3) / 1e9
-    n_sec = max(args.steps // 4, 3)
+    # per-operator split: an eager pass of the same step with events between
+    # the operators (the combine runs after the dispatch, as in the step)
+    def split_body(mark):
+        mark(0)
+        ep.moe_dispatch_layout(idx, w, E, R, L, stream)
+        mark(1)
+        ep.moe_dispatch(x, L, fmt, recv, recv_s, stream)
+        mark(2)
+        ep.moe_combine(y, L, w, out, stream)
+        mark(3)
+    lay, dis, com = tm.eager(split_body, n_sec, 4)
+    # each operator alone, graph-replayed after a flush (the layout is complete)
+    g_lay = tm.graph(lambda s: ep.moe_dispatch_layout(idx, w, E, R, L, s), n_sec)
+    g_dis = tm.graph(lambda s: ep.moe_dispatch(x, L, fmt, recv, recv_s, s), n_sec)
+    g_com = tm.graph(lambda s: ep.moe_combine(y, L, w, out, s), n_sec)
+    # dispatch + combine as a pair (graph-replayed; the combine pays the
+    # write-back of the dispatch's dirty receive rows)
+    g_pair = tm.graph(lambda s: (ep.moe_dispatch(x, L, fmt, recv, recv_s, s), ep.moe_combine(y, L, w, out, s)), n_sec)
+    s_dis = stream_dispatch(fmt)
+    s_com = tm.back_to_back(rotating(lambda s, o, i: ep.moe_combine(ys[i], L, w, o, s), outs), n_stream)
+    check(L, "after the per-operator passes")
+
     legs = set(LEGS) if args.legs == "all" else set() if args.legs == "none" else set(args.legs.split(","))
-
-    def timed(body, n, marks):
-        """n flushed repetitions of body(events) with `marks` events each;
-        the mean time between consecutive events in ms."""
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(marks)] for _ in range(n)]
-        for e in evs:
-            flush()
-            body(e)
-        torch.cuda.synchronize(dev)
-        return [statistics.mean(e[i].elapsed_time(e[i + 1]) for e in evs) for i in range(marks - 1)]
-
-    def pct(ms_list):
-        """p10 / p50 / p90 of per-repetition times, in us."""
-        q = statistics.quantiles(ms_list, n=10, method="inclusive") if len(ms_list) > 1 else [ms_list[0]] * 9
-        return {"p10": round(q[0] * 1e3, 2), "p50": round(statistics.median(ms_list) * 1e3, 2), "p90": round(q[8] * 1e3, 2)}
-
-    def hbm_op(us_ms, nbytes, **extra):
-        return {"us": round(us_ms * 1e3, 2), "bytes": nbytes, "GB/s": round(gbps(nbytes, us_ms), 1),
-                "frac": round(gbps(nbytes, us_ms) / peak, 4), **extra}
-
-    com_ms = statistics.mean(com)
-    achieved = ab["combine"] / (com_ms * 1e-3) / 1e9
     ops = {
-        "note": "per-operator times from an eager pass of the step with events between the operators",
+        "note": ("us: graph-replayed (one CUDA graph per figure, events at its two ends, L2 flushed before "
+                 "each replay, after warm-up replays); eager_us: eager launches with events between the "
+                 "operators; stream_us: per launch in one graph of 8 back-to-back launches over 4 rotating "
+                 "buffer sets (each launch's buffers untouched for the 3 launches before it, well over L2's "
+                 "size; frac_stream from it); back_to_back_us (low-latency legs): per launch, 8 launches on the "
+                 "same L2-resident buffers; frac: of the measured HBM copy rate, frac_spec: of the 8 TB/s "
+                 "datasheet HBM3e bandwidth"),
         "step_us": pct(tot),
-        "layout": {"us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"], "us_pct": pct(lay)},
-        "dispatch_bf16": hbm_op(statistics.mean(dis), ab["dispatch"],
-                                tokens_per_s=round(T / (statistics.mean(dis) * 1e-3), 1), us_pct=pct(dis)),
-        "combine": hbm_op(com_ms, ab["combine"], tokens_per_s=round(T / (com_ms * 1e-3), 1), us_pct=pct(com)),
+        "layout": {"us": round(statistics.mean(g_lay) * 1e3, 2), "us_pct": pct(g_lay),
+                   "eager_us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"]},
+        f"dispatch_{FORMAT_NAMES[fmt]}": hbm_op(ab[dkey], g_dis, dis, s_dis,
+                                                tokens_per_s=round(T / (statistics.mean(g_dis) * 1e-3), 1)),
+        "combine": hbm_op(ab["combine"], g_com, com, s_com, tokens_per_s=round(T / (statistics.mean(g_com) * 1e-3), 1),
+                          eager_note="eager_us: after the dispatch, inside the step"),
+        "dispatch_combine_pair": hbm_op(ab[dkey] + ab["combine"], g_pair),
     }
 
-    # FP8 and MXFP8 dispatch on the same layout (secondary figures)
-    for fmt, key, leg in ((ep.MOE_FORMAT_FP8, "dispatch_fp8", "fp8"), (ep.MOE_FORMAT_MXFP8, "dispatch_mxfp8", "mxfp8")):
-        if leg not in legs:
-            continue
-        rq, rs = ep.alloc_recv(L, H, fmt, device=dev)
+    # the step in the other receive format, graph-replayed like the timed steps
+    # (bf16 step: layout -> FP8 dispatch -> combine; FP8 step: the bf16 one)
+    if "formats" in legs:
+        ofmt = ep.MOE_FORMAT_BF16 if fmt else ep.MOE_FORMAT_FP8
+        oq, os_ = ep.alloc_recv(L, H, ofmt, device=dev)
+        g_other = tm.graph(lambda s: step_ops(s, ofmt, oq, os_), n_sec)
+        ob = ab["layout"] + ab[dispatch_key(ofmt)] + ab["combine"]
+        ops[f"step_{FORMAT_NAMES[ofmt]}"] = hbm_op(ob, g_other, step=step_label(ofmt),
+                                                   tokens_per_s=round(T / (statistics.mean(g_other) * 1e-3), 1))
+        del oq, os_
+        # each quantised format's dispatch alone on the same layout
+        for f in (ep.MOE_FORMAT_FP8, ep.MOE_FORMAT_MXFP8):
+            key = f"dispatch_{FORMAT_NAMES[f]}"
+            if key in ops:
+                continue
+            rq, rs = ep.alloc_recv(L, H, f, device=dev)
 
-        def body(e, fmt=fmt, rq=rq, rs=rs):
-            e[0].record(stream)
-            ep.moe_dispatch(x, L, fmt, rq, rs, stream)
-            e[1].record(stream)
-        ops[key] = hbm_op(timed(body, n_sec, 2)[0], ab[key])
-        del rq, rs
+            def body(mark, f=f, rq=rq, rs=rs):
+                mark(0)
+                ep.moe_dispatch(x, L, f, rq, rs, stream)
+                mark(1)
+            eg = tm.eager(body, n_sec, 2)[0]
+            gr = tm.graph(lambda s, f=f, rq=rq, rs=rs: ep.moe_dispatch(x, L, f, rq, rs, s), n_sec)
+            del rq, rs
+            ops[key] = hbm_op(ab[dispatch_key(f)], gr, eg, stream_dispatch(f),
+                              tokens_per_s=round(T / (statistics.mean(gr) * 1e-3), 1))
+        check(L, "after the format legs")
 
     # backward pair: gradients of the receive rows and of the output
     if "backward" in legs:
-        grad_recv = torch.empty_like(recv).normal_()
+        grad_recv = torch.empty(L.capacity, H, dtype=torch.bfloat16, device=dev).normal_()
         grad_out = torch.empty_like(out).normal_()
         grad_x = torch.empty_like(x)
         grad_y = torch.empty_like(y)
         grad_w = torch.empty_like(w)
 
-        def body(e):
-            e[0].record(stream)
+        def body(mark):
+            mark(0)
             ep.moe_dispatch_backward(grad_recv, L, grad_x, stream)
-            e[1].record(stream)
+            mark(1)
             ep.moe_combine_backward(grad_out, y, L, w, grad_y, grad_w, stream)
-            e[2].record(stream)
-        dbwd, cbwd = timed(body, n_sec, 3)
-        ops["dispatch_backward"] = hbm_op(dbwd, ab["dispatch_backward"])
-        ops["combine_backward"] = hbm_op(cbwd, ab["combine_backward"])
+            mark(2)
+        dbwd, cbwd = tm.eager(body, n_sec, 3)
+        gd = tm.graph(lambda s: ep.moe_dispatch_backward(grad_recv, L, grad_x, s), n_sec)
+        gc = tm.graph(lambda s: ep.moe_combine_backward(grad_out, y, L, w, grad_y, grad_w, s), n_sec)
+        ops["dispatch_backward"] = hbm_op(ab["dispatch_backward"], gd, dbwd)
+        ops["combine_backward"] = hbm_op(ab["combine_backward"], gc, cbwd)
         del grad_recv, grad_out, grad_x, grad_y, grad_w
-    st, flags = ep.moe_layout_read_status(L, stream)
-    if st != 0:
-        raise RuntimeError(f"device status {st} after the secondary legs")
+        check(L, "after the backward legs")
 
     # low-latency (decode) path: 128 tokens of the same shape, fixed capacity 128 per expert
     if "ll" in legs:
@@ -381,18 +518,26 @@ def run_ours(args, rank, world, local_rank):
         st_ll = torch.zeros(1, dtype=torch.int32, device=dev)
         out_ll = torch.empty(T_ll, H, dtype=torch.bfloat16, device=dev)
 
-        def body(e):
-            e[0].record(stream)
+        def body(mark):
+            mark(0)
             ep.moe_ll_dispatch(x_ll, idx_ll, E, T_ll, recv_ll, tpe_ll, slot_ll, st_ll, stream)
-            e[1].record(stream)
+            mark(1)
             ep.moe_ll_combine(recv_ll, slot_ll, w_ll, E, T_ll, out_ll, st_ll, stream)
-            e[2].record(stream)
-        lld, llc = timed(body, n_sec, 3)
+            mark(2)
+        lld, llc = tm.eager(body, n_sec, 3)
+        ll_d = lambda s: ep.moe_ll_dispatch(x_ll, idx_ll, E, T_ll, recv_ll, tpe_ll, slot_ll, st_ll, s)
+        ll_c = lambda s: ep.moe_ll_combine(recv_ll, slot_ll, w_ll, E, T_ll, out_ll, st_ll, s)
+        gd, gc = tm.graph(ll_d, n_sec), tm.graph(ll_c, n_sec)
+        # back to back on the same (L2-resident) buffers: the launch-to-launch time of a decode loop
+        bd, bc = tm.back_to_back([ll_d] * 8, n_stream), tm.back_to_back([ll_c] * 8, n_stream)
         if int(st_ll.item()) != 0:
             raise RuntimeError("low-latency path reported a device error")
         ll_bytes = 2 * T_ll * H + 2 * H * T_ll * K + 4 * T_ll * K    # rows read, one row per entry written
-        ops["ll_dispatch_T128"] = {"us": round(lld * 1e3, 2), "bytes": ll_bytes, "GB/s": round(gbps(ll_bytes, lld), 1)}
-        ops["ll_combine_T128"] = {"us": round(llc * 1e3, 2), "bytes": ll_bytes, "GB/s": round(gbps(ll_bytes, llc), 1)}
+        for key, g_, e_, b_ in (("ll_dispatch_T128", gd, lld, bd), ("ll_combine_T128", gc, llc, bc)):
+            ops[key] = {"us": round(statistics.mean(g_) * 1e3, 2), "us_pct": pct(g_),
+                        "eager_us": round(statistics.mean(e_) * 1e3, 2),
+                        "back_to_back_us": round(statistics.mean(b_) * 1e3, 2), "bytes": ll_bytes,
+                        "GB/s": round(gbps(ll_bytes, statistics.mean(g_)), 1), "bound": "latency"}
         del recv_ll
 
     # multi-source receive: all eight ranks' tokens of this shape at once (S = 8
@@ -407,29 +552,33 @@ def run_ours(args, rank, world, local_rank):
         recv_ms, _ = ep.alloc_recv(L_ms, H, False, device=dev)
         out_ms = torch.empty(S_ms * T, H, dtype=torch.bfloat16, device=dev)
 
-        def body(e):
-            e[0].record(stream)
+        def body(mark):
+            mark(0)
             ep.moe_dispatch_layout(idx_ms, w_ms, E, R, L_ms, stream)
-            e[1].record(stream)
+            mark(1)
             ep.moe_dispatch(x_ms, L_ms, False, recv_ms, None, stream)
-            e[2].record(stream)
+            mark(2)
             ep.moe_combine(y_ms, L_ms, w_ms, out_ms, stream)
-            e[3].record(stream)
-        msl, msd, msc = timed(body, max(args.steps // 10, 3), 4)
-        st, flags = ep.moe_layout_read_status(L_ms, stream)
-        if st != 0:
-            raise RuntimeError(f"device status {st} in the multi-source leg")
+            mark(3)
+        n_ms = max(10, n_sec // 4)
+        msl, msd, msc = tm.eager(body, n_ms, 4)
+        gl = tm.graph(lambda s: ep.moe_dispatch_layout(idx_ms, w_ms, E, R, L_ms, s), n_ms)
+        gd = tm.graph(lambda s: ep.moe_dispatch(x_ms, L_ms, False, recv_ms, None, s), n_ms)
+        gc = tm.graph(lambda s: ep.moe_combine(y_ms, L_ms, w_ms, out_ms, s), n_ms)
+        check(L_ms, "in the multi-source leg")
         ab_ms = algorithmic_bytes(S_ms * T, H, E, R, K, int(L_ms.tokens_per_rank.sum().item()),
                                   int(L_ms.expert_offset[E].item()), L_ms.capacity)
         ops["multi_source_S8"] = {"note": f"8 sources x {T} tokens, one region of {8 * T} rows per destination rank",
-                                  "layout_us": round(msl * 1e3, 2),
-                                  "dispatch_bf16": hbm_op(msd, ab_ms["dispatch"]),
-                                  "combine": hbm_op(msc, ab_ms["combine"])}
+                                  "layout": {"us": round(statistics.mean(gl) * 1e3, 2), "us_pct": pct(gl),
+                                             "eager_us": round(statistics.mean(msl) * 1e3, 2)},
+                                  "dispatch_bf16": hbm_op(ab_ms["dispatch"], gd, msd),
+                                  "combine": hbm_op(ab_ms["combine"], gc, msc)}
         del x_ms, y_ms, recv_ms, out_ms, L_ms
 
     # the other routing shapes: Zipf-skewed Qwen3-235B-like routing (one rank
     # receives nearly every token) and DeepSeek-16B-like routing over 32 ranks
-    # with a narrow hidden size; each an eager flushed step of its own
+    # with a narrow hidden size; each a graph-replayed step of its own plus its
+    # operators alone (bf16, FP8 and MXFP8 dispatch)
     if "workloads" in legs:
         wls = {}
         for name in OTHER_WORKLOADS:
@@ -445,54 +594,116 @@ def run_ours(args, rank, world, local_rank):
             recv_o, _ = ep.alloc_recv(L_o, Ho, False, device=dev)
             out_o = torch.empty(To, Ho, dtype=torch.bfloat16, device=dev)
 
-            def body(e):
-                e[0].record(stream)
+            def body(mark):
+                mark(0)
                 ep.moe_dispatch_layout(idx_o, w_o, Eo, Ro, L_o, stream)
-                e[1].record(stream)
+                mark(1)
                 ep.moe_dispatch(x_o, L_o, False, recv_o, None, stream)
-                e[2].record(stream)
+                mark(2)
                 ep.moe_combine(y_o, L_o, w_o, out_o, stream)
-                e[3].record(stream)
-            ol, od, oc = timed(body, n_sec, 4)
-            st, flags = ep.moe_layout_read_status(L_o, stream)
-            if st != 0:
-                raise RuntimeError(f"device status {st} in the {name} leg")
+                mark(3)
+            ol, od, oc = tm.eager(body, n_sec, 4)
+            gs = tm.graph(lambda s: (ep.moe_dispatch_layout(idx_o, w_o, Eo, Ro, L_o, s),
+                                     ep.moe_dispatch(x_o, L_o, False, recv_o, None, s),
+                                     ep.moe_combine(y_o, L_o, w_o, out_o, s)), n_sec)
+            gl = tm.graph(lambda s: ep.moe_dispatch_layout(idx_o, w_o, Eo, Ro, L_o, s), n_sec)
+            gd = tm.graph(lambda s: ep.moe_dispatch(x_o, L_o, False, recv_o, None, s), n_sec)
+            gc = tm.graph(lambda s: ep.moe_combine(y_o, L_o, w_o, out_o, s), n_sec)
+            check(L_o, f"in the {name} leg")
             tpr = L_o.tokens_per_rank.cpu()
             ab_o = algorithmic_bytes(To, Ho, Eo, Ro, Ko, int(tpr.sum()), int(L_o.expert_offset[Eo].item()),
                                      L_o.capacity)
-            wls[name] = {"shape": workload_label(wo), "n_pairs": int(tpr.sum()),
-                         "rows_per_rank_min_max": [int(tpr.min()), int(tpr.max())],
-                         "layout_us": round(ol * 1e3, 2),
-                         "dispatch_bf16": hbm_op(od, ab_o["dispatch"], tokens_per_s=round(To / (od * 1e-3), 1)),
-                         "combine": hbm_op(oc, ab_o["combine"], tokens_per_s=round(To / (oc * 1e-3), 1))}
-            del x_o, y_o, recv_o, out_o, L_o
+            tps = lambda g_: round(To / (statistics.mean(g_) * 1e-3), 1)
+            del recv_o
+            # back-to-back figures over rotating buffer sets, as for the step's shape
+            xs_o = [x_o] + [x_o.clone() for _ in range(NB - 1)]
+
+            def stream_o(f):
+                sets = [ep.alloc_recv(L_o, Ho, f, device=dev) for _ in range(NB)]
+                ms = tm.back_to_back(rotating(lambda s, b, i: ep.moe_dispatch(xs_o[i], L_o, f, b[0], b[1], s), sets),
+                               n_stream)
+                del sets
+                return ms
+            ys_o = [y_o] + [y_o.clone() for _ in range(NB - 1)]
+            outs_o = [out_o] + [torch.empty_like(out_o) for _ in range(NB - 1)]
+            sc = tm.back_to_back(rotating(lambda s, o, i: ep.moe_combine(ys_o[i], L_o, w_o, o, s), outs_o), n_stream)
+            del ys_o, outs_o
+            entry = {"shape": workload_label(wo), "n_pairs": int(tpr.sum()),
+                     "rows_per_rank_min_max": [int(tpr.min()), int(tpr.max())],
+                     "step": hbm_op(ab_o["layout"] + ab_o["dispatch"] + ab_o["combine"], gs, tokens_per_s=tps(gs),
+                                    step=step_label(0)),
+                     "layout": {"us": round(statistics.mean(gl) * 1e3, 2), "us_pct": pct(gl),
+                                "eager_us": round(statistics.mean(ol) * 1e3, 2)},
+                     "dispatch_bf16": hbm_op(ab_o["dispatch"], gd, od, stream_o(0), tokens_per_s=tps(gd)),
+                     "combine": hbm_op(ab_o["combine"], gc, oc, sc, tokens_per_s=tps(gc),
+                                       eager_note="eager_us: after the dispatch, inside the step")}
+            for f in (ep.MOE_FORMAT_FP8, ep.MOE_FORMAT_MXFP8):
+                rq, rs = ep.alloc_recv(L_o, Ho, f, device=dev)
+                gf = tm.graph(lambda s, f=f, rq=rq, rs=rs: ep.moe_dispatch(x_o, L_o, f, rq, rs, s), n_sec)
+                del rq, rs
+                entry[f"dispatch_{FORMAT_NAMES[f]}"] = hbm_op(ab_o[dispatch_key(f)], gf, None, stream_o(f),
+                                                              tokens_per_s=tps(gf))
+            del xs_o
+            check(L_o, f"in the {name} leg")
+            wls[name] = entry
+            del x_o, y_o, out_o, L_o
         ops["other_workloads"] = wls
 
-    # how many CTAs ("channels") the HBM-bound operators need: bf16 dispatch (one
-    # warp per CTA) and combine (256 threads per CTA) at fixed CTA counts
+    # how many CTAs ("channels") the HBM-bound operators need: the TMA-staged
+    # bf16 dispatch (one warp per CTA), combine (256 threads per CTA, 16-byte
+    # loads) and the TMA-staged combine (a producer warp stages the K rows,
+    # four warps reduce), graph-replayed at fixed CTA counts
     if "channels" in legs:
-        sweep = {"note": "GB/s at a fixed number of CTAs; default = the operator's own grid", "dispatch_bf16": {},
-                 "combine": {}}
+        sweep = {"note": "GB/s at a fixed number of CTAs (graph-replayed, flushed); default = the operator's own grid",
+                 "dispatch_bf16_tma": {}, "combine": {}, "combine_tma": {}}
+        bq, _ = ep.alloc_recv(L, H, False, device=dev)
         for n_cta in SWEEP_CTAS + (0,):
-            def body_d(e, n_cta=n_cta):
-                e[0].record(stream)
-                ep.moe_dispatch(x, L, False, recv, None, stream, num_channels=n_cta, variant=1)
-                e[1].record(stream)
-
-            def body_c(e, n_cta=n_cta):
-                e[0].record(stream)
-                ep.moe_combine(y, L, w, out, stream, num_channels=n_cta)
-                e[1].record(stream)
             key = str(n_cta) if n_cta else "default"
-            sweep["dispatch_bf16"][key] = round(gbps(ab["dispatch"], timed(body_d, 10, 2)[0]), 1)
-            sweep["combine"][key] = round(gbps(ab["combine"], timed(body_c, 10, 2)[0]), 1)
+            for name, fn, nb in (
+                    ("dispatch_bf16_tma", lambda s, c=n_cta: ep.moe_dispatch(x, L, False, bq, None, s, num_channels=c,
+                                                                         variant=1), ab["dispatch"]),
+                    ("combine", lambda s, c=n_cta: ep.moe_combine(y, L, w, out, s, num_channels=c), ab["combine"]),
+                    ("combine_tma", lambda s, c=n_cta: ep.moe_combine(y, L, w, out, s, num_channels=c, variant=1),
+                     ab["combine"])):
+                sweep[name][key] = round(gbps(nb, statistics.mean(tm.graph(fn, 10))), 1)
         ops["channel_sweep"] = sweep
+        del bq
 
-    e2e = run_e2e(args, inp, L, dev, ab, step_bytes) if (rank == 0 and "e2e" in legs) else None
+    e2e = run_e2e(args, inp, L, dev, fmt, step_bytes) if (rank == 0 and "e2e" in legs) else None
 
+    # roofline of the dominant kernel (the combine), timed inside the step
+    # (after the dispatch), plus the figures that bracket it
+    com_ms = statistics.mean(com)
+    achieved = gbps(ab["combine"], com_ms)
+    traffic, traffic_src = (committed_traffic("combine_dsv3_ncu") if args.workload in ("dsv3", "dsv3_fp8")
+                            else (None, "no committed capture of this shape"))
+    pair_ms = statistics.mean(g_pair)
+    roofline = {
+        "bound": "hbm", "kernel": f"combine_kernel<{K if K in (1, 2, 4, 6, 8) else 0}>",
+        "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+        "peak_source": (f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs, torch copy)" if peak_kind == "measured"
+                        else "fallback 6.8 TB/s"),
+        "frac_spec": round(achieved / SPEC_HBM_GBS, 4), "peak_spec": SPEC_HBM_GBS,
+        "traffic": traffic, "traffic_source": traffic_src,
+        "timing": ("combine between events in the eager per-operator pass, after the dispatch: its window "
+                   "includes the write-back of the dirty receive rows the dispatch leaves in L2 (up to ~100 MB); "
+                   "combine_alone is the same kernel graph-replayed after an L2 flush, pair the dispatch and "
+                   "the combine graph-replayed together, their bytes over their joint time"),
+        "algorithmic_bytes": ab["combine"],
+        "combine_alone": {"us": round(statistics.mean(g_com) * 1e3, 2),
+                          "frac": round(gbps(ab["combine"], statistics.mean(g_com)) / peak, 4),
+                          "frac_spec": round(gbps(ab["combine"], statistics.mean(g_com)) / SPEC_HBM_GBS, 4)},
+        "pair": {"kernels": "dispatch_wide_kernel + combine_kernel",
+                 "bytes": ab[dkey] + ab["combine"], "us": round(pair_ms * 1e3, 2),
+                 "achieved": round(gbps(ab[dkey] + ab["combine"], pair_ms), 1),
+                 "frac": round(gbps(ab[dkey] + ab["combine"], pair_ms) / peak, 4),
+                 "frac_spec": round(gbps(ab[dkey] + ab["combine"], pair_ms) / SPEC_HBM_GBS, 4)},
+    }
+
+    value = aggregate_gbps(step_bytes, ms_step, world)
     result = {
         "metric": METRIC,
-        "value": round(aggregate_gbps(step_bytes, ms_step, world), 1),
+        "value": round(value, 1),
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
@@ -501,24 +712,16 @@ def run_ours(args, rank, world, local_rank):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "bf16" if fmt == 0 else "e4m3+bf16",
         "data": f"synthetic (seeded N(0,1) activations, softmax top-{K} routing of N(0,1) logits"
                 + (f", Zipf s={wl.zipf_s} expert bias)" if wl.zipf_s else ")"),
-        "config": {"workload": workload_label(wl),
-                   "T": T, "H": H, "E": E, "R": R, "K": K, "n_pairs": n_pairs, "capacity": L.capacity,
-                   "step": "layout + bf16 dispatch + combine", "l2": "flushed between steps (256 MB write, then 256 MB read of another buffer)",
-                   "launch": "timed steps replay one CUDA graph (layout -> dispatch -> combine)",
-                   "parallelism": f"replicas x{world}"},
+        "config": step_config(wl, fmt, n_pairs, L.capacity, world),
+        "launch": "timed steps replay one CUDA graph (layout -> dispatch -> combine), events at its two ends",
+        "frac": round(value / world / peak, 4),
+        "frac_spec": round(value / world / SPEC_HBM_GBS, 4),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
         "ops": ops,
-        "roofline": {"bound": "hbm", "kernel": f"combine_kernel<{K if K in (1, 2, 4, 6, 8) else 0}>", "achieved": round(achieved, 1),
-                     "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind == "measured"
-                     else "fallback 6.8 TB/s",
-                     "traffic": committed_traffic("combine.cu", "combine_dsv3_ncu.md") if args.workload == WORKLOAD
-                     else None,
-                     "timing": "combine between events in the eager per-operator pass, after the dispatch",
-                     "algorithmic_bytes": ab["combine"]},
+        "roofline": roofline,
         "gpu_launches": 4 * args.steps,
         "clocks": clocks,
         "wall_s_timed_region": round(t_wall, 3),
@@ -528,7 +731,7 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
-def run_e2e(args, inp, L, dev, ab, step_bytes):
+def run_e2e(args, inp, L, dev, fmt, step_bytes):
     """Same step through the public API with host buffers: pinned host ->
     device copies of the inputs, the three calls, device -> host copy of the
     combine output and the per-expert counts, every step inside the timed
@@ -548,12 +751,12 @@ def run_e2e(args, inp, L, dev, ab, step_bytes):
              "w": torch.empty_like(inp.topk_w, device=dev), "y": torch.empty_like(inp.y, device=dev)}
             for _ in range(2)]
     out = torch.empty(wl.T, wl.H, dtype=torch.bfloat16, device=dev)
-    recv, _ = ep.alloc_recv(L, wl.H, False, device=dev)
+    recv, recv_s = ep.alloc_recv(L, wl.H, fmt, device=dev)
     comp = torch.cuda.current_stream(dev)
     copy = torch.cuda.Stream(dev)
     copied = [torch.cuda.Event() for _ in range(2)]
     consumed = [torch.cuda.Event() for _ in range(2)]
-    n = max(3, min(args.steps // 10, 50))
+    n = max(20, min(args.steps // 10, 50))
 
     def run(steps):
         for i in range(steps):
@@ -568,13 +771,13 @@ def run_e2e(args, inp, L, dev, ab, step_bytes):
             copied[i % 2].record(copy)
             comp.wait_event(copied[i % 2])
             ep.moe_dispatch_layout(b["idx"], b["w"], wl.E, wl.R, L, comp)
-            ep.moe_dispatch(b["x"], L, False, recv, None, comp)
+            ep.moe_dispatch(b["x"], L, fmt, recv, recv_s, comp)
             ep.moe_combine(b["y"], L, b["w"], out, comp)
             consumed[i % 2].record(comp)
             hout.copy_(out, non_blocking=True)
             hcnt.copy_(L.tokens_per_expert, non_blocking=True)
 
-    run(3)
+    run(max(3, args.warmup))
     torch.cuda.synchronize(dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
@@ -596,10 +799,10 @@ def run_e2e(args, inp, L, dev, ab, step_bytes):
 
 # ------------------------------------------------------------ CPU baselines
 
-def oracle_step_fn(wl, inp, T_s):
-    """One oracle pass (layout, bf16 dispatch, combine) over the first T_s
-    tokens of the workload; returns (callable, algorithmic bytes)."""
-    import numpy as np
+def oracle_step_fn(wl, inp, T_s, fmt=0):
+    """One oracle pass (layout, dispatch in the step's format, combine) over
+    the first T_s tokens of the workload; returns (callable, algorithmic
+    bytes, pairs, capacity)."""
     import oracle
     from combine_moe_dispatch_02_gb300.inputs import bf16_bits
     idx = inp.topk_idx[:T_s].numpy()
@@ -609,18 +812,20 @@ def oracle_step_fn(wl, inp, T_s):
     yb = bf16_bits(inp.y[: T_s * wl.K])
     Lo = oracle.layout(idx, w, wl.E, wl.R)
     ab = algorithmic_bytes(T_s, wl.H, wl.E, wl.R, wl.K, Lo.n_pairs, int(Lo.expert_offset[wl.E]), Lo.capacity)
+    disp = oracle.dispatch_fp8 if fmt else oracle.dispatch_bf16
 
     def run():
         L = oracle.layout(idx, w, wl.E, wl.R)
-        oracle.dispatch_bf16(xb, L)
+        disp(xb, L)
         oracle.combine(yb, L.expert_slot, w)
-    return run, ab["layout"] + ab["dispatch"] + ab["combine"]
+    return run, ab["layout"] + ab[dispatch_key(fmt)] + ab["combine"], Lo.n_pairs, Lo.capacity
 
 
 def cpu_baseline(wl, inp, budget_s=10.0):
     """The oracle as it stands, single-threaded, timed on this host over the
     full workload repeated until about `budget_s` seconds have passed."""
-    run, nbytes = oracle_step_fn(wl, inp, wl.T)
+    fmt = 1 if wl.fp8 else 0
+    run, nbytes, _, _ = oracle_step_fn(wl, inp, wl.T, fmt)
     run()  # warm-up
     t0 = time.perf_counter()
     n = 0
@@ -631,15 +836,36 @@ def cpu_baseline(wl, inp, budget_s=10.0):
             break
     dt = (time.perf_counter() - t0) / n
     return {"value": round(nbytes / dt / 1e9, 3), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "sample": f"full workload ({wl.T} tokens) x {n} passes of layout + bf16 dispatch + combine, "
-                      f"{dt:.3f} s each, 1 thread", "host_cpu": _cpu_name(), "host_cores": os.cpu_count()}
+            "sample": f"full workload ({wl.T} tokens) x {n} passes of {step_label(fmt)}, {dt:.3f} s each, 1 thread",
+            "host_cpu": cpu_model(), "host_cores": os.cpu_count()}
 
 
-def _cpu_name():
+# Arm CPU part numbers (MIDR) of the cores these hosts carry, for hosts whose
+# lscpu prints no model name
+_ARM_PARTS = {"0xd4f": "Neoverse-V2 (NVIDIA Grace)", "0xd40": "Neoverse-V1", "0xd0c": "Neoverse-N1",
+              "0xd49": "Neoverse-N2"}
+
+
+def cpu_model():
+    """The host's CPU model: lscpu's "Model name", else /proc/cpuinfo's."""
     try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name:"):
+                name = line.split(":", 1)[1].strip()
+                return _ARM_PARTS.get(name.lower(), name)
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        part = None
         for line in open("/proc/cpuinfo"):
-            if line.lower().startswith(("model name", "cpu part")):
+            key = line.split(":", 1)[0].strip().lower()
+            if key == "model name":
                 return line.split(":", 1)[1].strip()
+            if key == "cpu part" and part is None:
+                part = line.split(":", 1)[1].strip().lower()
+        if part:
+            return _ARM_PARTS.get(part, f"Arm CPU part {part}")
     except OSError:
         pass
     import platform
@@ -653,14 +879,15 @@ def run_reference(args):
     import oracle
     oracle.build()
     wl = WORKLOADS[args.workload]
+    fmt = 1 if wl.fp8 else 0
     inp = make_inputs(wl, seed=0)
-    probe, _ = oracle_step_fn(wl, inp, 128)
+    probe, _, _, _ = oracle_step_fn(wl, inp, 128, fmt)
     t0 = time.perf_counter()
     probe()
     per_tok = (time.perf_counter() - t0) / 128
     target = 60.0 / max(args.steps + args.warmup, 1)         # about a minute in total
     T_s = int(max(32, min(wl.T, target / max(per_tok, 1e-9))))
-    run, nbytes = oracle_step_fn(wl, inp, T_s)
+    run, nbytes, n_pairs, capacity = oracle_step_fn(wl, inp, T_s, fmt)
     for _ in range(args.warmup):
         run()
     times = []
@@ -672,12 +899,12 @@ def run_reference(args):
     v = round(nbytes / dt / 1e9, 3)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic", "config": {"workload": f"DeepSeek-V3 shape, first {T_s} of {wl.T} tokens per step",
-                                            "T_sample": T_s, "H": wl.H, "E": wl.E, "R": wl.R, "K": wl.K},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "bf16" if fmt == 0 else "e4m3+bf16", "data": "synthetic",
+            "config": step_config(wl, fmt, n_pairs, capacity, 1, T_sample=T_s),
             "cpu_baseline": {"value": v, "unit": "GB/s", "kind": "oracle", "cores": 1,
-                             "sample": f"{T_s} tokens of the 4096-token workload per step, 1 thread",
-                             "host_cpu": _cpu_name()},
+                             "sample": f"{T_s} of the workload's {wl.T} tokens per step, 1 thread",
+                             "host_cpu": cpu_model(), "host_cores": os.cpu_count()},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 

@@ -53,3 +53,27 @@ def test_deepseek_v3_totals():
     assert ab["dispatch"] == 369_125_376
     assert ab["combine"] == 528_744_448
     assert ab["dispatch_fp8"] == ab["dispatch_mxfp8"] == 218_836_384
+
+
+def test_reference_arm_config_equals_the_gpu_arms():
+    """The reference (CPU oracle) arm reports the same `config` object as the
+    GPU arm when its per-step sample is the whole workload: built by the same
+    function from the same pair count and capacity."""
+    import argparse
+    import oracle
+    from combine_moe_dispatch_02_gb300.inputs import WORKLOADS, make_inputs
+    wl = WORKLOADS["tiny"]
+    ref = bench.run_reference(argparse.Namespace(workload="tiny", steps=3, warmup=3, gpus=1))
+    inp = make_inputs(wl)
+    L = oracle.layout(inp.topk_idx.numpy(), inp.topk_w.numpy(), wl.E, wl.R)
+    assert ref["config"] == bench.step_config(wl, 0, L.n_pairs, L.capacity, 1)
+    assert ref["config"]["T"] == wl.T and "first" not in ref["config"]["workload"]
+    assert not ref["cpu_baseline"]["host_cpu"].startswith("0x")
+
+
+def test_config_names_a_partial_sample():
+    from combine_moe_dispatch_02_gb300.inputs import WORKLOADS
+    wl = WORKLOADS["dsv3"]
+    cfg = bench.step_config(wl, 0, 100, 800, 1, T_sample=100)
+    assert "first 100 of 4096 tokens" in cfg["workload"] and cfg["T"] == 100
+    assert bench.step_config(wl, 1, 21643, 32768, 1)["step"].startswith("layout + FP8")

@@ -46,10 +46,15 @@ def test_bench_json_line_contract():
     assert d["gpu_launches"] == 4 * d["steps"]
     clk = d["clocks"]
     assert {"sm_mhz", "sm_max_mhz", "reasons"} <= set(clk)
+    assert e2e["steps"] >= 20
+    assert 0.3 < rf["frac_spec"] < rf["frac"]
+    assert rf["pair"]["bytes"] == d["ops"]["dispatch_bf16"]["bytes"] + rf["algorithmic_bytes"]
+    assert 0.3 < rf["pair"]["frac"] < 1.5 and 0.3 < rf["combine_alone"]["frac"] < 1.5
+    assert rf["traffic"] is None or rf["traffic_source"].startswith("profiles/")
     ops = d["ops"]
     for key in ("layout", "dispatch_bf16", "combine"):
-        assert ops[key]["us"] > 0
-    for key in ("dispatch_bf16", "combine"):
+        assert ops[key]["us"] > 0 and ops[key]["eager_us"] > 0
+    for key in ("dispatch_bf16", "combine", "dispatch_combine_pair"):
         assert ops[key]["bytes"] > 0 and 0.2 < ops[key]["frac"] < 1.5
 
 
@@ -60,3 +65,18 @@ def test_bench_other_workload_as_the_step():
     assert "32 ranks" in cfg["workload"] and d["roofline"]["kernel"] == "combine_kernel<6>"
     assert d["value"] > 0 and "e2e" not in d
     assert d["roofline"]["traffic"] is None            # the committed capture is of the DeepSeek-V3 shape
+
+
+def test_bench_fp8_step_and_format_legs():
+    """--workload dsv3_fp8 times layout -> FP8 dispatch -> combine as the
+    step; the format leg adds the bf16 step and the FP8 / MXFP8 dispatches."""
+    d = _run("--legs", "formats", "--workload", "dsv3_fp8")
+    assert d["dtype"] == "e4m3+bf16" and d["config"]["step"].startswith("layout + FP8")
+    ops = d["ops"]
+    assert ops["dispatch_fp8"]["bytes"] == 218_836_384 and ops["dispatch_mxfp8"]["bytes"] == 218_836_384
+    assert ops["step_bf16"]["us"] > ops["dispatch_combine_pair"]["us"] > 0
+    for key in ("dispatch_fp8", "dispatch_mxfp8"):
+        assert 0.3 < ops[key]["frac"] < 1.5 and ops[key]["eager_us"] > 0
+    # the step's bytes: layout + FP8 dispatch + combine
+    step_bytes = ops["layout"]["bytes"] + 218_836_384 + d["roofline"]["algorithmic_bytes"]
+    assert abs(d["value"] * 1e9 * d["ms_per_step"] * 1e-3 / step_bytes - 1) < 1e-3
