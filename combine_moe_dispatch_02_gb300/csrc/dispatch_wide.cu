@@ -232,8 +232,11 @@ __device__ __forceinline__ void wide_emit(const WideArgs& a, int32_t t, int32_t 
 
 // FMT 0: bf16 rows; 1: FP8 with fp32 1x128 scales; 2: MXFP8 (E8M0 1x32
 // scales).  ONE: the default grid, exactly one item per warp (warp w takes
-// item w), straight-line code whose registers (FP8 63, MXFP8 48, bf16 39)
-// let four, five and six CTAs of 256 threads share an SM.  Otherwise each
+// item w), straight-line code: FP8 in 63 registers (four CTAs of 256 threads
+// per SM; bounded to five it spills 28 bytes and measured 1-2 us slower at
+// two of three shapes), MXFP8 and bf16 bounded to six CTAs per SM (40
+// registers, no spill; MXFP8 0.5 us faster at the DeepSeek-V3 shape than at
+// four, the same elsewhere).  Otherwise each
 // warp takes a contiguous run of items with one item in registers: the next
 // item's loads are issued as soon as the current one is quantised (bf16: once
 // it is stored), before its stores, so the load latency overlaps the stores
@@ -242,7 +245,7 @@ __device__ __forceinline__ void wide_emit(const WideArgs& a, int32_t t, int32_t 
 // slower on GB300 at every shape: the registers they need cost occupancy or
 // spill.
 template <int FMT, bool ONE>
-__global__ void __launch_bounds__(kWideThreads, 4)
+__global__ void __launch_bounds__(kWideThreads, (ONE && FMT != 1) ? 6 : 4)
 dispatch_wide_kernel(WideArgs a) {
     pdl_wait();
     const int lane = threadIdx.x & 31;
