@@ -635,7 +635,7 @@ dispatch_lsu_kernel(DispatchArgs a) {
 cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
                             void* recv_x, void* recv_scales, cudaStream_t stream,
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
-                            uint64_t timeout_ns) {
+                            uint64_t timeout_ns, bool x_ready) {
     if (L->T == 0) return cudaSuccess;
     // The default and variant 4: the 32-byte vector kernel (dispatch_wide.cu);
     // where the pointers or the row pitch do not keep 32-byte alignment, the
@@ -643,7 +643,7 @@ cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout*
     // kernel for FP8 / MXFP8 (variant 2)
     if (variant == 4 || variant == 0) {
         if (dispatch_wide_supported(x, hidden, format, recv_x))
-            return launch_dispatch_wide(x, hidden, L, format, recv_x, recv_scales, stream, num_channels);
+            return launch_dispatch_wide(x, hidden, L, format, recv_x, recv_scales, stream, num_channels, x_ready);
         variant = format == MOE_FORMAT_BF16 ? 1 : 2;
     }
     DispatchArgs a;

@@ -86,12 +86,11 @@ struct WideItem {
     int32_t seg;
 };
 
-__device__ __forceinline__ void wide_load(WideItem& it, const WideArgs& a, int32_t t, int32_t seg, int lane,
-                                          int32_t prev_t, int32_t prev_slot) {
+// The item's source columns only (x is an input of the call; the slots are
+// the layout's output).
+__device__ __forceinline__ void wide_load_x(WideItem& it, const WideArgs& a, int32_t t, int32_t seg, int lane) {
     it.t = t;
     it.seg = seg;
-    // the slot row is fetched once per token the warp meets (warp-uniform test)
-    it.slot = t == prev_t ? prev_slot : (lane < a.R ? __ldg(a.recv_slot + static_cast<int64_t>(t) * a.R + lane) : -1);
     const int col = seg * kWideSeg + lane * kWideLaneCols;
     const uint8_t* src = a.x + (static_cast<int64_t>(t) * a.H + col) * 2;
     if (col < a.H) {
@@ -106,6 +105,18 @@ __device__ __forceinline__ void wide_load(WideItem& it, const WideArgs& a, int32
 #pragma unroll
         for (int j = 8; j < 16; ++j) it.w[j] = 0u;
     }
+}
+
+// The lane's entry of the token's recv_slot row (rank = lane; -1 past R).
+__device__ __forceinline__ int32_t wide_slot(const WideArgs& a, int32_t t, int lane) {
+    return lane < a.R ? __ldg(a.recv_slot + static_cast<int64_t>(t) * a.R + lane) : -1;
+}
+
+__device__ __forceinline__ void wide_load(WideItem& it, const WideArgs& a, int32_t t, int32_t seg, int lane,
+                                          int32_t prev_t, int32_t prev_slot) {
+    // the slot row is fetched once per token the warp meets (warp-uniform test)
+    it.slot = t == prev_t ? prev_slot : wide_slot(a, t, lane);
+    wide_load_x(it, a, t, seg, lane);
 }
 
 // Largest magnitude of the lane's 32 values as a bf16 bit pattern; clears
@@ -244,14 +255,33 @@ __device__ __forceinline__ void wide_emit(const WideArgs& a, int32_t t, int32_t 
 // registers and 12 bytes of spill).  Two items in registers per warp measured
 // slower on GB300 at every shape: the registers they need cost occupancy or
 // spill.
-template <int FMT, bool ONE>
+//
+// EARLY (with ONE; moe_dispatch_with_layout only): x was complete before the
+// layout's first kernel, so the warp loads its item -- and quantises it --
+// before the dependency wait, while the layout still runs; only the slots
+// and the stores wait for it.
+template <int FMT, bool ONE, bool EARLY>
 __global__ void __launch_bounds__(kWideThreads, (ONE && FMT != 1) ? 6 : 4)
 dispatch_wide_kernel(WideArgs a) {
-    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int64_t warp_id = static_cast<int64_t>(blockIdx.x) * kWideWarps + (threadIdx.x >> 5);
     bool bad = false;
-    if constexpr (ONE) {
+    if constexpr (EARLY) {
+        static_assert(ONE, "early loads take the one-item grid");
+        const bool live = warp_id < a.n_items;
+        const int32_t t = live ? static_cast<int32_t>(warp_id / a.nseg) : 0;
+        const int32_t seg = live ? static_cast<int32_t>(warp_id - static_cast<int64_t>(t) * a.nseg) : 0;
+        uint32_t codes[8];
+        uint32_t sw = 0;
+        WideItem it;
+        if (live) {
+            wide_load_x(it, a, t, seg, lane);
+            sw = wide_quant<FMT>(it, codes);
+        }
+        pdl_wait();
+        if (live) wide_emit<FMT>(a, t, seg, wide_slot(a, t, lane), it.w, codes, sw, lane, bad);
+    } else if constexpr (ONE) {
+        pdl_wait();
         if (warp_id < a.n_items) {
             const int32_t t = static_cast<int32_t>(warp_id / a.nseg);
             const int32_t seg = static_cast<int32_t>(warp_id - static_cast<int64_t>(t) * a.nseg);
@@ -262,6 +292,7 @@ dispatch_wide_kernel(WideArgs a) {
             wide_emit<FMT>(a, t, seg, it.slot, it.w, codes, sw, lane, bad);
         }
     } else {
+        pdl_wait();
         const int64_t n_warps = static_cast<int64_t>(gridDim.x) * kWideWarps;
         const int64_t i0 = a.n_items * warp_id / n_warps;
         const int64_t i1 = a.n_items * (warp_id + 1) / n_warps;
@@ -305,7 +336,7 @@ bool dispatch_wide_supported(const void* x, int32_t hidden, int32_t format, cons
 }
 
 cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format, void* recv_x,
-                                 void* recv_scales, cudaStream_t stream, int32_t num_channels) {
+                                 void* recv_scales, cudaStream_t stream, int32_t num_channels, bool x_ready) {
     if (L->T == 0) return cudaSuccess;
     WideArgs a;
     a.x = reinterpret_cast<const uint8_t*>(x);
@@ -333,14 +364,19 @@ cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_la
     if (grid < 1) grid = 1;
     if (grid > INT32_MAX) return cudaErrorInvalidConfiguration;
     const dim3 g(static_cast<unsigned>(grid)), b(kWideThreads);
-    if (grid == need) {           // one item per warp
-        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, true>, g, b, 0, stream, a);
-        if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, true>, g, b, 0, stream, a);
-        return launch_pdl(dispatch_wide_kernel<0, true>, g, b, 0, stream, a);
+    if (grid == need && x_ready) {        // one item per warp, loaded before the dependency wait
+        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, true, true>, g, b, 0, stream, a);
+        if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, true, true>, g, b, 0, stream, a);
+        return launch_pdl(dispatch_wide_kernel<0, true, true>, g, b, 0, stream, a);
     }
-    if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, false>, g, b, 0, stream, a);
-    if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, false>, g, b, 0, stream, a);
-    return launch_pdl(dispatch_wide_kernel<0, false>, g, b, 0, stream, a);
+    if (grid == need) {                   // one item per warp
+        if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, true, false>, g, b, 0, stream, a);
+        if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, true, false>, g, b, 0, stream, a);
+        return launch_pdl(dispatch_wide_kernel<0, true, false>, g, b, 0, stream, a);
+    }
+    if (format == MOE_FORMAT_MXFP8) return launch_pdl(dispatch_wide_kernel<2, false, false>, g, b, 0, stream, a);
+    if (format == MOE_FORMAT_FP8) return launch_pdl(dispatch_wide_kernel<1, false, false>, g, b, 0, stream, a);
+    return launch_pdl(dispatch_wide_kernel<0, false, false>, g, b, 0, stream, a);
 }
 
 }  // namespace moe

@@ -522,10 +522,16 @@ struct FinalArgs {
     int32_t *tokens_per_rank, *rank_offset;
     int32_t *recv_slot, *expert_slot, *recv_src_token, *expert_src_row;
     float* expert_weight;
+    int32_t early_trigger;      // let the next kernel become resident at once (see below)
 };
 
 __global__ void __launch_bounds__(kFinalizeThreads)
 layout_finalize_kernel(FinalArgs a) {
+    // With early_trigger the next kernel's CTAs may become resident while the
+    // scan still runs; they wait for this grid before using its outputs, so
+    // this only matters for work they can do without them (the dispatch of
+    // moe_dispatch_with_layout loads and quantises its rows meanwhile).
+    if (a.early_trigger) pdl_trigger();
     extern __shared__ int32_t sm[];
     const int E1 = a.E + 1;
     int32_t* s_eoff = sm;                                    // [E+1]
@@ -560,7 +566,7 @@ layout_finalize_kernel(FinalArgs a) {
     const uint32_t epoch = header ? ld_relaxed_gpu(&a.ws.hdr->epoch) : 0u;
 
     pdl_wait();
-    pdl_trigger();          // one wave of CTAs: the dispatch grid may become resident now
+    if (!a.early_trigger) pdl_trigger();    // one wave of CTAs: the dispatch grid may become resident now
     // the scan's per-entry ranks (loaded for every entry, so that they do not
     // wait for the ids) and, inside expert_offsets, its totals
     int32_t er_r[kFinalizePerThread], pr_r[kFinalizePerThread];
@@ -765,7 +771,7 @@ LayoutWs layout_workspace(const moe_layout* L) {
 }
 
 cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const moe_layout* L,
-                          cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags) {
+                          cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags, bool early_trigger) {
     const LayoutWs ws = layout_workspace(L);
     ScanArgs sa;
     sa.topk_idx = topk_idx;
@@ -800,6 +806,7 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     fa.tokens_per_rank = L->tokens_per_rank; fa.rank_offset = L->rank_offset;
     fa.recv_slot = L->recv_slot; fa.expert_slot = L->expert_slot; fa.recv_src_token = L->recv_src_token;
     fa.expert_src_row = L->expert_src_row; fa.expert_weight = L->expert_weight;
+    fa.early_trigger = early_trigger ? 1 : 0;
     int64_t blocks = (static_cast<int64_t>(L->T) + kFinalizeTokens - 1) / kFinalizeTokens;
     if (blocks < 1) blocks = 1;
     const size_t smem2 = sizeof(int32_t) * (2 * (static_cast<size_t>(L->E) + 1) +

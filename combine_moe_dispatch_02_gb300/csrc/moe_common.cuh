@@ -248,15 +248,20 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 
 // Launch helpers implemented in the per-operator translation units.
 namespace moe {
+// early_trigger: the kernel after the layout may become resident while the
+// scan runs (moe_dispatch_with_layout); x_ready: x was complete before the
+// layout's first kernel, so the dispatch may read it before its dependency
+// wait (moe_dispatch_with_layout only).
 cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const moe_layout* L,
-                          cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags);
+                          cudaStream_t stream, uint64_t timeout_ns, uint32_t debug_flags,
+                          bool early_trigger = false);
 cudaError_t launch_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
                             void* recv_x, void* recv_scales, cudaStream_t stream,
                             int32_t num_channels, int32_t stages, int32_t chunk_bytes, int32_t variant,
-                            uint64_t timeout_ns);
+                            uint64_t timeout_ns, bool x_ready = false);
 bool dispatch_wide_supported(const void* x, int32_t hidden, int32_t format, const void* recv_x);
 cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format, void* recv_x,
-                                 void* recv_scales, cudaStream_t stream, int32_t num_channels);
+                                 void* recv_scales, cudaStream_t stream, int32_t num_channels, bool x_ready);
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
                            uint64_t timeout_ns);

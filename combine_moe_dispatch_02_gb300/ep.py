@@ -40,7 +40,7 @@ MOE_FORMAT_MXFP8 = 2
 
 EXPORTED = ["moe_layout_bytes", "moe_layout_init", "moe_layout_sources_bytes", "moe_layout_init_sources",
             "moe_dispatch_layout", "moe_dispatch_layout_noalloc",
-            "moe_dispatch", "moe_combine", "moe_dispatch_backward", "moe_combine_backward",
+            "moe_dispatch", "moe_dispatch_with_layout", "moe_combine", "moe_dispatch_backward", "moe_combine_backward",
             "moe_ll_dispatch", "moe_ll_combine",
             "moe_layout_read_status", "moe_status_string", "moe_device_sm_count"]
 
@@ -105,6 +105,9 @@ def lib() -> ctypes.CDLL:
         L.moe_dispatch.restype = ctypes.c_int
         L.moe_dispatch.argtypes = [P, i32, ctypes.POINTER(moe_layout), i32, P, P, P,
                                    ctypes.POINTER(moe_tuning)]
+        L.moe_dispatch_with_layout.restype = ctypes.c_int
+        L.moe_dispatch_with_layout.argtypes = [P, P, i32, i32, ctypes.POINTER(moe_layout), P, i32, i32, P, P, P,
+                                               ctypes.POINTER(moe_tuning)]
         L.moe_combine.restype = ctypes.c_int
         L.moe_combine.argtypes = [P, i32, ctypes.POINTER(moe_layout), P, P, P, ctypes.POINTER(moe_tuning)]
         L.moe_dispatch_backward.restype = ctypes.c_int
@@ -254,6 +257,20 @@ def moe_dispatch(x: torch.Tensor, L: Layout, fmt, recv_x: torch.Tensor,
     assert recv_x.is_contiguous() and (recv_scales is None or recv_scales.is_contiguous())
     _check(lib().moe_dispatch(_ptr(x), x.shape[-1], ctypes.byref(L.c), int(fmt), _ptr(recv_x),
                               _ptr(recv_scales), _stream(stream), _tuning(**tuning)), "moe_dispatch")
+
+
+def moe_dispatch_with_layout(topk_idx: torch.Tensor, topk_w: torch.Tensor | None, num_experts: int,
+                             num_ranks: int, L: Layout, x: torch.Tensor, fmt, recv_x: torch.Tensor,
+                             recv_scales: torch.Tensor | None = None, stream=None, **tuning) -> None:
+    """moe_dispatch_layout followed by moe_dispatch in one call (the dispatch
+    may read x while the layout is computed)."""
+    assert topk_idx.dtype == torch.int32 and topk_idx.is_contiguous()
+    assert topk_w is None or (topk_w.dtype == torch.float32 and topk_w.is_contiguous())
+    assert x.dtype == torch.bfloat16 and x.is_contiguous()
+    assert recv_x.is_contiguous() and (recv_scales is None or recv_scales.is_contiguous())
+    _check(lib().moe_dispatch_with_layout(_ptr(topk_idx), _ptr(topk_w), num_experts, num_ranks, ctypes.byref(L.c),
+                                          _ptr(x), x.shape[-1], int(fmt), _ptr(recv_x), _ptr(recv_scales),
+                                          _stream(stream), _tuning(**tuning)), "moe_dispatch_with_layout")
 
 
 def moe_combine(y: torch.Tensor, L: Layout, topk_w: torch.Tensor, out: torch.Tensor, stream=None,

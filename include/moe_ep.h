@@ -264,15 +264,36 @@ moe_status moe_dispatch_layout_noalloc(const int32_t* topk_idx, const float* top
  *     q = E4M3(x * 2^-se), round to nearest even, saturating at 448.
  * x is bf16 [T, hidden]; hidden % 8 == 0 (hidden % 128 == 0 for both FP8
  * formats); x, recv_x 16-byte aligned, recv_scales 4-byte aligned.  Rows
- * past rank_offset[R] are not written.  bf16 (default kernel): each CTA is an
- * independent channel over a contiguous range of (token, column chunk)
- * items: TMA bulk loads of the chunk into shared memory, then one TMA bulk
- * store per destination row; no grid-wide synchronisation (Hybrid-EP news
- * article, "Technical Structure": each CUDA block an independent channel).
- * FP8 and MXFP8 (default kernel): warps quantise 512-column segments in
- * registers and store 16 codes per lane to every destination row. */
+ * past rank_offset[R] are not written.  Default kernel (every format, when x
+ * and recv_x are 32-byte aligned): each warp moves one 1024-column segment of
+ * one token -- two 32-byte loads per lane, the FP8 / MXFP8 codes computed in
+ * registers -- and writes it with one 32-byte store per lane to every
+ * destination row; no grid-wide synchronisation.  16-byte aligned calls take
+ * the staged kernel for bf16 (each CTA an independent channel: TMA bulk loads
+ * of a row chunk into shared memory, then one TMA bulk store per destination
+ * row; Hybrid-EP news article, "Technical Structure") and the 16-byte vector
+ * kernel for FP8 / MXFP8. */
 moe_status moe_dispatch(const uint16_t* x, int32_t hidden, const moe_layout* L, int32_t format,
                         void* recv_x, void* recv_scales, void* stream, const moe_tuning* tuning);
+
+/* moe_dispatch_layout followed by moe_dispatch, in one call: the same
+ * arguments and checks as the two calls, the same results in L, recv_x and
+ * recv_scales (the dispatch uses num_experts, num_ranks and L exactly as the
+ * layout call leaves them).  Dispatch sends each token to the ranks its
+ * layout assigns ("Inside the Nebius + PyTorch DeepSeek V3 recipe",
+ * "Mixture-of-experts and wide expert parallelism"), so the two always come
+ * in this order.  Because x is an input of this one call -- complete before
+ * its first kernel starts, like topk_idx -- the dispatch may read x while the
+ * layout is still being computed: for bf16 and MXFP8 rows the default kernel
+ * becomes resident while the layout runs, and each warp loads (MXFP8: and
+ * quantises) its segment of x before it waits for the slots.  With two
+ * separate calls the dispatch cannot, since the caller may write x between
+ * them.  FP8 rows (no gain measured) run as the two calls do.  tuning
+ * applies to both parts as in the two calls. */
+moe_status moe_dispatch_with_layout(const int32_t* topk_idx, const float* topk_w, int32_t num_experts,
+                                    int32_t num_ranks, moe_layout* L, const uint16_t* x, int32_t hidden,
+                                    int32_t format, void* recv_x, void* recv_scales, void* stream,
+                                    const moe_tuning* tuning);
 
 /* Combine: the expert outputs back to each token's position, weighted by the
  * router ("Inside the Nebius + PyTorch DeepSeek V3 recipe", "Mixture-of-

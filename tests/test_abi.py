@@ -75,6 +75,14 @@ def test_operator_calls_reject_bad_arguments_on_the_host(lib):
     assert lib.moe_dispatch(p, 128, ctypes.byref(L), 2, p, None, None, None) == ep.MOE_ERR_INVALID_ARG  # scales missing
     assert lib.moe_combine(p, 12, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
     assert lib.moe_combine(None, 64, ctypes.byref(L), p, p, None, None) == ep.MOE_ERR_INVALID_ARG
+    # layout + dispatch in one call: the checks of both (nothing is enqueued when either fails)
+    with_layout = lib.moe_dispatch_with_layout
+    assert with_layout(p, p, 16, 4, ctypes.byref(L), p, 64, 0, p, None, None, None) == ep.MOE_ERR_INVALID_ARG  # E
+    assert with_layout(p, p, 8, 4, ctypes.byref(L), p, 12, 0, p, None, None, None) == ep.MOE_ERR_INVALID_ARG   # hidden
+    assert with_layout(p, p, 8, 4, ctypes.byref(L), p, 64, 1, p, p, None, None) == ep.MOE_ERR_INVALID_ARG     # fp8 hidden
+    assert with_layout(None, p, 8, 4, ctypes.byref(L), p, 64, 0, p, None, None, None) == ep.MOE_ERR_INVALID_ARG  # ids
+    assert with_layout(p, p, 8, 4, ctypes.byref(L), p, 64, 0, p, None, None,
+                       ctypes.byref(ep.moe_tuning(variant=5))) == ep.MOE_ERR_INVALID_ARG
 
 
 def test_more_calls_reject_bad_arguments_on_the_host(lib):
