@@ -3,9 +3,11 @@
 
 One step = dispatch layout (2 kernels) -> dispatch -> combine over the
 DeepSeek-V3-shaped workload: 4096 tokens, hidden 7168, 256 experts over 8
-virtual ranks, top-8 (seeded synthetic routing and activations).  The
-dispatch writes bf16 rows, or FP8 E4M3 rows with 1x128 fp32 scales under
-``--workload dsv3_fp8``.  Inputs are resident in HBM; L2 is flushed (a 256 MB
+virtual ranks, top-8 (seeded synthetic routing and activations), made with
+the library's moe_dispatch_with_layout call (layout and dispatch in one
+call) and moe_combine; the three separate calls are timed as
+ops.step_separate_calls.  The dispatch writes bf16 rows, or FP8 E4M3 rows
+with 1x128 fp32 scales under ``--workload dsv3_fp8``.  Inputs are resident in HBM; L2 is flushed (a 256 MB
 write, then a 256 MB read of another buffer) between timed steps, outside the
 CUDA-event brackets.  Prints one JSON line.
 
@@ -83,6 +85,11 @@ def dispatch_key(fmt: int) -> str:
 def step_label(fmt: int) -> str:
     return {0: "layout + bf16 dispatch + combine",
             1: "layout + FP8 E4M3 dispatch (1x128 fp32 scales) + combine of bf16 expert outputs"}[int(fmt)]
+
+
+# the calls a step makes: the layout and the dispatch in one moe_dispatch_with_layout call (its
+# dispatch may read x while the layout is computed), then moe_combine
+STEP_CALLS = "moe_dispatch_with_layout (layout + dispatch in one call) + moe_combine"
 
 
 def step_config(wl, fmt, n_pairs, capacity, world, T_sample=None):
@@ -335,6 +342,10 @@ def run_ours(args, rank, world, local_rank):
             raise RuntimeError(f"device status {st} ({ep.moe_status_string(st)}) flags {flags:#x} {what}")
 
     def step_ops(s, f=fmt, rq=recv, rs=recv_s):
+        ep.moe_dispatch_with_layout(idx, w, E, R, L, x, f, rq, rs, s)
+        ep.moe_combine(y, L, w, out, s)
+
+    def step_ops_separate(s, f=fmt, rq=recv, rs=recv_s):
         ep.moe_dispatch_layout(idx, w, E, R, L, s)
         ep.moe_dispatch(x, L, f, rq, rs, s)
         ep.moe_combine(y, L, w, out, s)
@@ -435,6 +446,8 @@ def run_ours(args, rank, world, local_rank):
     # dispatch + combine as a pair (graph-replayed; the combine pays the
     # write-back of the dispatch's dirty receive rows)
     g_pair = tm.graph(lambda s: (ep.moe_dispatch(x, L, fmt, recv, recv_s, s), ep.moe_combine(y, L, w, out, s)), n_sec)
+    # the same step through the three separate calls
+    g_sep = tm.graph(step_ops_separate, n_sec)
     s_dis = stream_dispatch(fmt)
     s_com = tm.back_to_back(rotating(lambda s, o, i: ep.moe_combine(ys[i], L, w, o, s), outs), n_stream)
     check(L, "after the per-operator passes")
@@ -456,6 +469,8 @@ def run_ours(args, rank, world, local_rank):
         "combine": hbm_op(ab["combine"], g_com, com, s_com, tokens_per_s=round(T / (statistics.mean(g_com) * 1e-3), 1),
                           eager_note="eager_us: after the dispatch, inside the step"),
         "dispatch_combine_pair": hbm_op(ab[dkey] + ab["combine"], g_pair),
+        "step_separate_calls": hbm_op(step_bytes, g_sep, calls="moe_dispatch_layout + moe_dispatch + moe_combine",
+                                      tokens_per_s=round(T / (statistics.mean(g_sep) * 1e-3), 1)),
     }
 
     # the step in the other receive format, graph-replayed like the timed steps
@@ -717,6 +732,7 @@ def run_ours(args, rank, world, local_rank):
                 + (f", Zipf s={wl.zipf_s} expert bias)" if wl.zipf_s else ")"),
         "config": step_config(wl, fmt, n_pairs, L.capacity, world),
         "launch": "timed steps replay one CUDA graph (layout -> dispatch -> combine), events at its two ends",
+        "calls": STEP_CALLS,
         "frac": round(value / world / peak, 4),
         "frac_spec": round(value / world / SPEC_HBM_GBS, 4),
         "tokens_per_s": round(world * T / (ms_step * 1e-3), 1),
@@ -733,7 +749,7 @@ def run_ours(args, rank, world, local_rank):
 
 def run_e2e(args, inp, L, dev, fmt, step_bytes):
     """Same step through the public API with host buffers: pinned host ->
-    device copies of the inputs, the three calls, device -> host copy of the
+    device copies of the inputs, the step's calls, device -> host copy of the
     combine output and the per-expert counts, every step inside the timed
     region.  Two device buffer sets: the inputs of step i+1 are copied on a
     copy stream while step i computes and copies its result back, as a
@@ -770,8 +786,7 @@ def run_e2e(args, inp, L, dev, fmt, step_bytes):
                 b["y"].copy_(hy, non_blocking=True)
             copied[i % 2].record(copy)
             comp.wait_event(copied[i % 2])
-            ep.moe_dispatch_layout(b["idx"], b["w"], wl.E, wl.R, L, comp)
-            ep.moe_dispatch(b["x"], L, fmt, recv, recv_s, comp)
+            ep.moe_dispatch_with_layout(b["idx"], b["w"], wl.E, wl.R, L, b["x"], fmt, recv, recv_s, comp)
             ep.moe_combine(b["y"], L, b["w"], out, comp)
             consumed[i % 2].record(comp)
             hout.copy_(out, non_blocking=True)
