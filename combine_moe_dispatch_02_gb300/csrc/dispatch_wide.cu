@@ -39,6 +39,7 @@
 // hidden % 16 == 0); otherwise it falls back to the 16-byte vector kernel.
 #include <climits>
 
+#include "fastdiv.h"
 #include "fp8_quant.cuh"
 #include "moe_common.cuh"
 
@@ -61,7 +62,21 @@ struct WideArgs {
     int32_t nseg;                // segments per row
     int64_t n_items;             // T * nseg
     uint32_t* status;
+    FastDiv seg_div;             // division by nseg
+    int32_t items_fit_u32;       // every warp index of the one-item grid is below 2^32
 };
+
+// Token and segment of item i (one-item grids).
+__device__ __forceinline__ void item_coords(const WideArgs& a, int64_t i, int32_t& t, int32_t& seg) {
+    if (a.items_fit_u32) {
+        const uint32_t q = fastdiv(static_cast<uint32_t>(i), a.seg_div);
+        t = static_cast<int32_t>(q);
+        seg = static_cast<int32_t>(static_cast<uint32_t>(i) - q * static_cast<uint32_t>(a.nseg));
+    } else {
+        t = static_cast<int32_t>(i / a.nseg);
+        seg = static_cast<int32_t>(i - static_cast<int64_t>(t) * a.nseg);
+    }
+}
 
 __device__ __forceinline__ void ld_v8(uint32_t* r, const void* p) {
     asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -164,12 +179,12 @@ __device__ __forceinline__ float wide_quant_fp8(uint32_t (&w)[16], uint32_t (&co
         return s;
     }
     const float r = block_recip(s);
+    const uint64_t r2 = pack_f32x2(r, r), ns2 = pack_f32x2(-s, -s);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float v0 = div_mag_by_scale(bf16_lo(w[2 * i]), s, r);
-        const float v1 = div_mag_by_scale(bf16_hi(w[2 * i]), s, r);
-        const float v2 = div_mag_by_scale(bf16_lo(w[2 * i + 1]), s, r);
-        const float v3 = div_mag_by_scale(bf16_hi(w[2 * i + 1]), s, r);
+    for (int i = 0; i < 8; ++i) {     // the quotients two at a time (packed fp32)
+        float v0, v1, v2, v3;
+        unpack_f32x2(div_mag_by_scale_x2(bf16x2_to_f32x2(w[2 * i]), r2, ns2), v0, v1);
+        unpack_f32x2(div_mag_by_scale_x2(bf16x2_to_f32x2(w[2 * i + 1]), r2, ns2), v2, v3);
         codes[i] |= e4m3x2(v0, v1) | (e4m3x2(v2, v3) << 16);
     }
     return s;
@@ -183,10 +198,12 @@ __device__ __forceinline__ uint32_t wide_quant_mx(uint32_t (&w)[16], uint32_t (&
     for (int j = 0; j < 16; ++j) acc = __vmaxu2(acc, w[j] & 0x7fff7fffu);
     const int se = mx_shared_exp(max(acc & 0xffffu, acc >> 16));
     const float mul = mx_inv_scale(se);
+    const uint64_t mul2 = pack_f32x2(mul, mul);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const float v0 = __fmul_rn(bf16_lo(w[2 * i]), mul), v1 = __fmul_rn(bf16_hi(w[2 * i]), mul);
-        const float v2 = __fmul_rn(bf16_lo(w[2 * i + 1]), mul), v3 = __fmul_rn(bf16_hi(w[2 * i + 1]), mul);
+    for (int i = 0; i < 8; ++i) {     // the products two at a time (packed fp32)
+        float v0, v1, v2, v3;
+        unpack_f32x2(mul_f32x2(bf16x2_to_f32x2(w[2 * i]), mul2), v0, v1);
+        unpack_f32x2(mul_f32x2(bf16x2_to_f32x2(w[2 * i + 1]), mul2), v2, v3);
         codes[i] = e4m3x2(v0, v1) | (e4m3x2(v2, v3) << 16);
     }
     return static_cast<uint32_t>(se + 127);
@@ -269,8 +286,8 @@ dispatch_wide_kernel(WideArgs a) {
     if constexpr (EARLY) {
         static_assert(ONE, "early loads take the one-item grid");
         const bool live = warp_id < a.n_items;
-        const int32_t t = live ? static_cast<int32_t>(warp_id / a.nseg) : 0;
-        const int32_t seg = live ? static_cast<int32_t>(warp_id - static_cast<int64_t>(t) * a.nseg) : 0;
+        int32_t t = 0, seg = 0;
+        if (live) item_coords(a, warp_id, t, seg);
         uint32_t codes[8];
         uint32_t sw = 0;
         WideItem it;
@@ -283,8 +300,8 @@ dispatch_wide_kernel(WideArgs a) {
     } else if constexpr (ONE) {
         pdl_wait();
         if (warp_id < a.n_items) {
-            const int32_t t = static_cast<int32_t>(warp_id / a.nseg);
-            const int32_t seg = static_cast<int32_t>(warp_id - static_cast<int64_t>(t) * a.nseg);
+            int32_t t, seg;
+            item_coords(a, warp_id, t, seg);
             uint32_t codes[8];
             WideItem it;
             wide_load(it, a, t, seg, lane, -1, -1);
@@ -348,6 +365,8 @@ cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_la
     a.nseg = (hidden + kWideSeg - 1) / kWideSeg;
     a.n_items = static_cast<int64_t>(L->T) * a.nseg;
     a.status = L->status;
+    a.seg_div = make_fastdiv(static_cast<uint32_t>(a.nseg));
+    a.items_fit_u32 = a.n_items + kWideWarps <= (int64_t{1} << 32) ? 1 : 0;
     // Default grid: one item per warp (the last CTA may hold fewer).  The
     // block scheduler then balances the tokens' unequal destination counts
     // CTA by CTA, and no warp of a CTA waits for a sibling with more items.

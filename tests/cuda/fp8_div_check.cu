@@ -9,7 +9,11 @@
 //   magnitude:  moe::div_mag_by_scale(|x|, s, r) vs __fdiv_rn(|x|, s) under
 //               the same exactness condition, and the E4M3 code of that
 //               quotient with the sign bit of x OR'ed in vs the code of
-//               __fdiv_rn(x, s), everywhere.
+//               __fdiv_rn(x, s), everywhere;
+//   packed:     moe::div_mag_by_scale_x2 on the pair (|x|, |x'|), x' another
+//               bf16 value, vs moe::div_mag_by_scale on each half, bit for
+//               bit everywhere (the packed fp32 instructions round each half
+//               like the scalar ones).
 // The first few quotient and code mismatches are recorded.  Every index is
 // bounded by the array sizes.
 #include <cstdint>
@@ -62,6 +66,14 @@ __global__ void div_check_kernel(const uint16_t* amax_bits, int n_amax, unsigned
         if (in_range && __float_as_uint(qm_fast) != __float_as_uint(__fdiv_rn(m, s))) atomicAdd(&counters[5], 1ull);
         const uint32_t cm = (moe::e4m3x2(qm_fast, 0.0f) & 0xffu) | ((xb >> 8) & 0x80u);
         if (cm != c_ieee) atomicAdd(&counters[6], 1ull);
+        float m2 = fabsf(__uint_as_float(((xb * 40503u) & 0xffffu) << 16));   // another bf16 value
+        if (!(m2 <= 0x1.fffffep127f)) m2 = m;                                   // finite ones only
+        float p0, p1;
+        moe::unpack_f32x2(moe::div_mag_by_scale_x2(moe::pack_f32x2(m, m2), moe::pack_f32x2(r, r),
+                                                   moe::pack_f32x2(-s, -s)), p0, p1);
+        if (__float_as_uint(p0) != __float_as_uint(qm_fast) ||
+            __float_as_uint(p1) != __float_as_uint(moe::div_mag_by_scale(m2, s, r)))
+            atomicAdd(&counters[7], 1ull);
     }
     const unsigned warp_n = __reduce_add_sync(0xffffffffu, local_n);
     if ((threadIdx.x & 31) == 0) atomicAdd(&counters[2], static_cast<unsigned long long>(warp_n));
@@ -70,7 +82,8 @@ __global__ void div_check_kernel(const uint16_t* amax_bits, int n_amax, unsigned
 }  // namespace
 
 // counters: [quotient mismatches, code mismatches, pairs checked, scale mismatches,
-//            reciprocal mismatches, magnitude-quotient mismatches, sign-OR code mismatches];
+//            reciprocal mismatches, magnitude-quotient mismatches, sign-OR code mismatches,
+//            packed-quotient mismatches];
 // examples: 2 * max_examples records of 4 words.
 extern "C" int fp8_div_check(const uint16_t* amax_bits, int n_amax, unsigned long long* counters,
                              uint32_t* examples, int max_examples) {

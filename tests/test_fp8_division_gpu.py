@@ -6,7 +6,8 @@ value x with |x| <= amax, for a few thousand block maxima spread over the
 whole bf16 exponent range: scales and reciprocals agree bit for bit, the
 quotients wherever the method is claimed exact, and the E4M3 codes
 everywhere; the same for the magnitude form (quotient of |x|, sign bit of x
-OR'ed into the code) that the wide dispatch kernel uses."""
+OR'ed into the code) that the wide dispatch kernel uses, whose packed
+two-value form must equal the scalar one bit for bit."""
 import ctypes
 import os
 import subprocess
@@ -39,7 +40,7 @@ def divcheck():
 
 def _run(divcheck, pats):
     amax = torch.tensor(sorted(pats), dtype=torch.int32).to(torch.int16).cuda()
-    counters = torch.zeros(7, dtype=torch.int64, device="cuda")
+    counters = torch.zeros(8, dtype=torch.int64, device="cuda")
     ex = torch.zeros(2 * 16 * 4, dtype=torch.int32, device="cuda")
     rc = divcheck.fp8_div_check(amax.data_ptr(), amax.numel(), counters.data_ptr(), ex.data_ptr(), 16)
     assert rc == 0
@@ -47,7 +48,7 @@ def _run(divcheck, pats):
 
 
 def test_scale_and_reciprocal_for_every_bf16_block_max(divcheck):
-    (_, _, _, scale_bad, recip_bad, _, _), _ = _run(divcheck, range(0x0001, 0x7F80))
+    (_, _, _, scale_bad, recip_bad, _, _, _), _ = _run(divcheck, range(0x0001, 0x7F80))
     assert scale_bad == 0 and recip_bad == 0
 
 
@@ -59,10 +60,11 @@ def test_fast_quotient_matches_ieee_division(divcheck):
     pats |= {e << 7 for e in range(1, 255)}
     pats |= {(e << 7) | 0x7F for e in range(0, 255)}
     pats |= {0x0001, 0x0080, 0x7F7F, 0x3F80, 0x4000, 0x43E0}
-    (q_bad, code_bad, n, scale_bad, recip_bad, mag_bad, sign_bad), ex = _run(divcheck, pats)
+    (q_bad, code_bad, n, scale_bad, recip_bad, mag_bad, sign_bad, packed_bad), ex = _run(divcheck, pats)
     assert n > 20_000_000                       # pairs inside the fast scale range
     assert q_bad == 0, ex[0][:min(q_bad, 16)]
     assert code_bad == 0, ex[1][:min(code_bad, 16)]
     assert scale_bad == 0 and recip_bad == 0
     # the wide dispatch kernel quantises |x| and ORs the sign of x into the code
     assert mag_bad == 0 and sign_bad == 0
+    assert packed_bad == 0
