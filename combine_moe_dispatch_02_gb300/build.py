@@ -17,7 +17,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libmoe_ep.so")
-SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "dispatch_wide.cu", "combine.cu", "backward.cu", "ll.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "layout.cu", "dispatch.cu", "dispatch_wide.cu", "combine.cu", "gather_wide.cu", "backward.cu", "ll.cu",
+           "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -265,6 +265,9 @@ combine_tma_kernel(CombineArgs a, uint64_t timeout_ns) {
 cudaError_t launch_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, const moe_layout* L,
                                      uint16_t* grad_x, cudaStream_t stream, int32_t num_channels) {
     if (L->T == 0) return cudaSuccess;
+    if (gather_wide_supported(grad_recv, grad_x, hidden))
+        return launch_gather_wide(grad_recv, L->recv_slot, nullptr, L->T, L->R, L->capacity, hidden, grad_x,
+                                  L->status, stream, num_channels);
     CombineArgs a;
     a.y = reinterpret_cast<const uint4*>(grad_recv);
     a.expert_slot = L->recv_slot;
@@ -318,6 +321,9 @@ cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* 
     a.T = L->T; a.K = L->K; a.H8 = hidden / 8;
     a.n_rows = static_cast<int64_t>(L->T) * L->K;
     a.status = L->status;
+    if (variant == 4 && gather_wide_supported(y, out, hidden))
+        return launch_gather_wide(y, L->expert_slot, topk_w, L->T, L->K, a.n_rows, hidden, out, L->status, stream,
+                                  num_channels);
     if (variant == 1 && L->K <= kTmaMaxK) {
         const size_t smem = align_up(16 * kTmaStages + sizeof(TmaStageMeta) * kTmaStages, 128) +
                             static_cast<size_t>(kTmaStages) * L->K * kTmaCE * 2;

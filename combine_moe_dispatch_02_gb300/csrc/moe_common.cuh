@@ -215,6 +215,21 @@ __device__ __forceinline__ void st_stream_v4(uint4* p, uint4 v) {
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
 
+// 32-byte forms (sm_100+; the address must be 32-byte aligned).
+__device__ __forceinline__ void ld_stream_v8(uint32_t (&r)[8], const void* p) {
+    asm volatile("ld.global.nc.L1::no_allocate.v8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+                   "=r"(r[7])
+                 : "l"(p));
+}
+
+__device__ __forceinline__ void st_stream_v8(void* p, const uint32_t (&r)[8]) {
+    asm volatile("st.global.cs.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 :: "l"(p), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]),
+                    "r"(r[7])
+                 : "memory");
+}
+
 // Programmatic dependent launch ---------------------------------------------
 //
 // The layout and dispatch kernels are launched with programmatic stream
@@ -265,6 +280,13 @@ cudaError_t launch_dispatch_wide(const uint16_t* x, int32_t hidden, const moe_la
 cudaError_t launch_combine(const uint16_t* y, int32_t hidden, const moe_layout* L, const float* topk_w,
                            uint16_t* out, cudaStream_t stream, int32_t num_channels, int32_t variant,
                            uint64_t timeout_ns);
+// 32-byte gather (gather_wide.cu): out[t] = bf16(fma chain over the valid
+// slots of row t, ascending k, weights w or 1).  Needs y and out 32-byte
+// aligned and hidden % 16 == 0 (gather_wide_supported).
+bool gather_wide_supported(const void* y, const void* out, int32_t hidden);
+cudaError_t launch_gather_wide(const uint16_t* y, const int32_t* slot, const float* w, int32_t T, int32_t K,
+                               int64_t n_rows, int32_t hidden, uint16_t* out, uint32_t* status,
+                               cudaStream_t stream, int32_t num_channels);
 cudaError_t launch_dispatch_backward(const uint16_t* grad_recv, int32_t hidden, const moe_layout* L,
                                      uint16_t* grad_x, cudaStream_t stream, int32_t num_channels);
 cudaError_t launch_combine_backward(const uint16_t* grad_out, const uint16_t* y, int32_t hidden, const moe_layout* L,

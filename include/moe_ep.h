@@ -82,7 +82,8 @@ typedef struct moe_tuning {
                                   32-byte vector loads / stores, a lane per 32 columns (needs
                                   x and recv_x 32-byte aligned and, for bf16, hidden % 16 == 0;
                                   otherwise it runs as 1 for bf16 and as 2 for FP8 / MXFP8;
-                                  combine treats 4 as 0)                                         */
+                                  combine: the 32-byte gather, one warp per 512-column segment,
+                                  with the same alignment rule, else as 0)                       */
     uint64_t wait_timeout_ns;  /* bound on every device-side wait; 0 = 1 second                   */
     uint32_t debug_flags;      /* MOE_DEBUG_* test hooks                                          */
     uint32_t reserved2;
@@ -304,7 +305,11 @@ moe_status moe_dispatch_with_layout(const int32_t* topk_idx, const float* topk_w
  * multiply-add chain starting from 0 in ascending k.  y is bf16 [T*K, hidden]
  * in expert-major row order (row expert_offset[e] + j is expert e's j-th
  * entry); out is bf16 [T, hidden]; a token with every entry masked gets +0.
- * hidden % 8 == 0; y and out 16-byte aligned. */
+ * hidden % 8 == 0; y and out 16-byte aligned.  moe_tuning.variant 4 takes the
+ * 32-byte gather (one warp per 512-column segment of a token, the valid
+ * slots found by one ballot; needs y and out 32-byte aligned and hidden % 16
+ * == 0, else it runs as 0).  Every variant gives the same bits; the default
+ * measured fastest for the combine's dense rows. */
 moe_status moe_combine(const uint16_t* y, int32_t hidden, const moe_layout* L,
                        const float* topk_w, uint16_t* out, void* stream, const moe_tuning* tuning);
 
@@ -337,7 +342,11 @@ moe_status moe_ll_combine(const uint16_t* y, const int32_t* ll_slot, const float
  * r = 0..R-1 with recv_slot[t,r] >= 0 of grad_recv[recv_slot[t,r], :]),
  * accumulated in fp32 in ascending r (0 for a token sent nowhere).
  * grad_recv is bf16 [capacity, hidden] (the gradient of the receive rows);
- * grad_x is bf16 [T, hidden].  hidden % 8 == 0, 16-byte aligned rows.
+ * grad_x is bf16 [T, hidden].  hidden % 8 == 0, 16-byte aligned rows.  With
+ * grad_recv and grad_x 32-byte aligned and hidden % 16 == 0 it runs the
+ * 32-byte gather of moe_combine's variant 4: each token's valid ranks come
+ * from one ballot over its recv_slot row; otherwise the 16-byte gather of
+ * moe_combine.  Both give the same bits.
  * Training is the pages' workload (Hybrid-EP news article, "Efficiency
  * Numbers"); they do not describe the backward pass: this is the adjoint of
  * the forward definition. */

@@ -21,7 +21,7 @@ def _gpu():
     oracle.build()
 
 
-def _run(idx, w, E, R, H, seed, capacity=None):
+def _run(idx, w, E, R, H, seed, capacity=None, **tuning):
     from combine_moe_dispatch_02_gb300 import ep
     T, K = idx.shape
     g = torch.Generator().manual_seed(seed)
@@ -34,7 +34,7 @@ def _run(idx, w, E, R, H, seed, capacity=None):
     gx = torch.empty(T, H, dtype=torch.bfloat16, device="cuda")
     gy = torch.full((T * K, H), -1.0, dtype=torch.bfloat16, device="cuda")
     gw = torch.full((T, K), 7.0, dtype=torch.float32, device="cuda")
-    ep.moe_dispatch_backward(grad_recv.cuda(), L, gx)
+    ep.moe_dispatch_backward(grad_recv.cuda(), L, gx, **tuning)
     ep.moe_combine_backward(grad_out.cuda(), y.cuda(), L, w_d, gy, gw)
     st = ep.moe_layout_read_status(L)
     Lo = oracle.layout(idx.numpy(), w.numpy(), E, R, capacity)
@@ -70,7 +70,21 @@ def test_backward_parity_workloads(name):
     (517, 136, 16, 4, 3, 0.2, True, 1),
     (300, 64, 64, 32, 12, 0.1, False, 2),     # K > 8: entries in groups of 8; R = 32
     (200, 8200, 16, 4, 4, 0.0, False, 3),
+    (400, 784, 64, 64, 8, 0.1, False, 4),     # R = 64: two 32-rank windows; a 272-column last segment
+    (257, 2064, 256, 256, 8, 0.0, False, 5),  # R = 256, one expert per rank: eight windows
 ])
 def test_backward_edge_cases(T, H, E, R, K, mask, dups, seed):
     idx = random_routing(T, K, E, seed, mask_frac=mask, allow_duplicates=dups)
+    _run(idx, random_weights(T, K, seed), E, R, H, seed + 10)
+
+
+@pytest.mark.parametrize("T,H,E,R,K,seed", [
+    (4096, 7168, 256, 8, 8, 6),               # DeepSeek-V3 shape: ~5 ranks per token, two batches of rows
+    (700, 1024, 64, 32, 6, 7),                # 32 ranks, about six of them per token
+    (300, 1040, 16, 4, 2, 8),                 # at most two ranks: one batch; a 16-column last segment
+])
+def test_dispatch_backward_gather(T, H, E, R, K, seed):
+    """The 32-byte gather of the dispatch backward (rows 32-byte aligned,
+    hidden % 16 == 0): bit for bit the oracle's add chain."""
+    idx = random_routing(T, K, E, seed)
     _run(idx, random_weights(T, K, seed), E, R, H, seed + 10)

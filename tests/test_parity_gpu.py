@@ -66,6 +66,27 @@ def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed, variant):
     assert_parity(g, o, fp8=fp8)
 
 
+@pytest.mark.parametrize("T,H,E,R,K,mask,seed", [
+    (777, 144, 16, 4, 3, 0.1, 30),            # one partial 512-column segment, one batch of rows
+    (1000, 784, 32, 8, 6, 0.2, 31),           # a 272-column last segment, masked entries
+    (300, 96, 64, 4, 16, 0.05, 32),           # K = 16: six batches per token
+    (4096, 64, 1024, 256, 32, 0.0, 33),       # K = 32: one full 32-slot window
+])
+def test_combine_gather(T, H, E, R, K, mask, seed):
+    """The combine as the 32-byte gather (variant 4) against the oracle, bit
+    for bit."""
+    idx = random_routing(T, K, E, seed, mask_frac=mask)
+    w = random_weights(T, K, seed)
+    g_ = torch.Generator().manual_seed(seed + 1)
+    x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
+    y = torch.randn(T * K, H, generator=g_).to(torch.bfloat16)
+    g = gpu_run(x, idx, w, y, E, R, variant=4)
+    o = oracle_run(x, idx, w, y, E, R)
+    assert g["status"] == 0 and o["status"] == 0
+    assert_parity(g, o)
+    assert np.array_equal(g["out"], o["out"])
+
+
 @pytest.mark.parametrize("T,H,E,R,K,mask,fp8,seed", [
     (262144, 8, 256, 8, 8, 0.0, False, 20),    # 1,024 scan tiles: the flag look-back at length
     (100003, 16, 64, 4, 6, 0.05, False, 21),   # ragged last tile, masked entries
