@@ -6,15 +6,19 @@
 // lands at row e * cap + j of recv [E, cap, H], j = the entry's position among
 // e's entries in (t,k) order, so the experts can run on fixed-size inputs.
 //
-// One launch, no workspace: decode batches are small (T * K <= 4096 entries
-// here), so every CTA loads the whole routing into shared memory and computes
-// all the positions itself (warp-aggregated ranks with per-warp histograms, as
-// in the layout scan, then a scan across warps).  A CTA owns a range of
-// tokens: it reads each token row once (16-byte vectors in registers; the
-// first row's loads are issued before the ranking, so their latency hides
-// behind it) and writes it to every destination row of the token.  CTA 0 also
-// writes the slot map and the per-expert counts.  The combine for this layout
-// is the regular weighted gather over the slot map (combine.cu).
+// One launch, no workspace.  A CTA owns a range of tokens and needs only the
+// rows of its own entries: row(t,k) = e * cap + j with j = #{earlier entries
+// of expert e}.  It counts the entries before its first token per expert
+// (shared-memory atomics over a histogram; T * K <= 4096 entries, all of a
+// thread's id loads in flight at once), then one warp walks its own entries
+// in order, 32 at a time: lanes with the same expert find each other with
+// one match instruction, take base + their rank among them, and the group's
+// lowest lane advances the count.  No CTA ranks the whole batch.  CTA 0 also
+// counts every entry for tokens_per_expert and the status word.  Each token
+// row is read once (16-byte vectors in registers; the first row's loads are
+// issued before the counting, so their latency hides behind it) and written
+// to every destination row of the token.  The combine for this layout is the
+// regular weighted gather over the slot map (combine.cu).
 #include "moe_common.cuh"
 
 namespace moe {
@@ -22,8 +26,9 @@ namespace moe {
 namespace {
 
 constexpr int kLLThreads = 256;
-constexpr int kLLWarps = kLLThreads / 32;
 constexpr int kLLVecs = 4;                    // 16-byte vectors per thread per column group (8192 columns)
+constexpr int kLLMaxEntries = 4096;           // T * K
+constexpr int kLLIdsPerThread = kLLMaxEntries / kLLThreads;
 
 struct LLArgs {
     const uint4* x;              // [T, H/8]
@@ -36,7 +41,9 @@ struct LLArgs {
 };
 
 // Column group [c0, c0 + kLLVecs * kLLThreads) of token t's row (16-byte
-// vectors; t < 0 or columns past the row give zeros).
+// vectors; t < 0 or columns past the row give zeros).  32-byte vectors
+// measured no faster here: a CTA's writes are bound by its SM's store path to
+// L2 (about 112 KB per token at 62 GB/s per SM), not by store instructions.
 __device__ __forceinline__ void load_group(const LLArgs& a, int t, int c0, int tid, uint4 (&v)[kLLVecs]) {
 #pragma unroll
     for (int j = 0; j < kLLVecs; ++j) {
@@ -49,73 +56,79 @@ __global__ void __launch_bounds__(kLLThreads)
 ll_dispatch_kernel(LLArgs a) {
     extern __shared__ int32_t sm[];
     const int n = a.T * a.K;
-    int32_t* s_e = sm;                          // [n]: expert of entry i, or -1
-    int32_t* s_pos = s_e + n;                   // [n]: position within the warp's segment, then row
-    int32_t* s_hist = s_pos + n;                // [warps][E]
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    pdl_wait();
-    // this CTA's tokens; the first row's first column group is loaded now
+    // this CTA's tokens and entries [i_begin, i_end)
     const int t_begin = static_cast<int>(static_cast<int64_t>(a.T) * blockIdx.x / gridDim.x);
     const int t_end = static_cast<int>(static_cast<int64_t>(a.T) * (blockIdx.x + 1) / gridDim.x);
+    const int i_begin = t_begin * a.K, i_end = t_end * a.K, m = i_end - i_begin;
+    const bool first = blockIdx.x == 0;        // also counts every entry: tokens_per_expert, status
+    int32_t* s_count = sm;                      // [E]: entries of e before the current one
+    int32_t* s_total = s_count + a.E;           // [E] (CTA 0): all entries of e
+    int32_t* s_own = s_total + a.E;             // [m]: expert of each own entry (-1: masked or bad), then its row
+    __shared__ uint32_t s_flags;
+    pdl_wait();
     uint4 v[kLLVecs];
     load_group(a, t_begin < t_end ? t_begin : -1, 0, tid, v);
 
-    bool bad_id = false;
-    for (int i = tid; i < n; i += kLLThreads) {
-        int e = a.topk_idx[i];
-        if (e < -1 || e >= a.E) { bad_id = true; e = -1; }
-        s_e[i] = e;
+    // the ids this CTA needs (those before its last token; CTA 0: all of them)
+    const int limit = first ? n : i_end;
+    int32_t e_in[kLLIdsPerThread];
+#pragma unroll
+    for (int u = 0; u < kLLIdsPerThread; ++u) {
+        const int i = tid + u * kLLThreads;
+        e_in[u] = i < limit ? __ldg(a.topk_idx + i) : -1;
     }
-    for (int i = tid; i < kLLWarps * a.E; i += kLLThreads) s_hist[i] = 0;
+    for (int e = tid; e < 2 * a.E; e += kLLThreads) s_count[e] = 0;
+    if (tid == 0) s_flags = 0u;
+    __syncthreads();
+    bool bad_id = false;
+#pragma unroll
+    for (int u = 0; u < kLLIdsPerThread; ++u) {
+        const int i = tid + u * kLLThreads;
+        if (i >= limit) break;
+        int e = e_in[u];
+        if (e < -1 || e >= a.E) { bad_id = true; e = -1; }     // counted as masked
+        if (e >= 0 && i < i_begin) atomicAdd(&s_count[e], 1);
+        if (e >= 0 && first) atomicAdd(&s_total[e], 1);
+        if (i >= i_begin && i < i_end) s_own[i - i_begin] = e;
+    }
+    if (bad_id) atomicOr(&s_flags, MOE_DEVERR_EXPERT_ID);
     __syncthreads();
 
-    // positions inside each warp's contiguous segment (ballot per id bit)
-    const int seg = ((n + kLLWarps - 1) / kLLWarps + 31) / 32 * 32;
-    const int nbits = 32 - __clz(max(a.E - 1, 1));
-    int32_t* my_hist = s_hist + warp * a.E;
-    const uint32_t lt = lanemask_lt();
-    for (int c = 0; c * 32 < seg; ++c) {
-        const int i = warp * seg + c * 32 + lane;
-        const int e = i < n ? s_e[i] : -1;
-        uint32_t peers = __ballot_sync(0xffffffffu, e >= 0);
-        if (e < 0) peers = ~peers;
-        for (int b = 0; b < nbits; ++b) {
-            const bool bit = (e >> b) & 1;
-            const uint32_t bb = __ballot_sync(0xffffffffu, bit);
-            peers &= bit ? bb : ~bb;
+    // own entries in (t,k) order, 32 at a time: base count + rank among equal experts
+    if (warp == 0) {
+        const uint32_t lt = lanemask_lt();
+        bool overflow = false;
+        for (int q0 = 0; q0 < m; q0 += 32) {
+            const int q = q0 + lane;
+            const int e = q < m ? s_own[q] : -1;
+            const uint32_t peers = __match_any_sync(0xffffffffu, e);
+            const int base = e >= 0 ? s_count[e] : 0;
+            __syncwarp();
+            int32_t row = -1;
+            if (e >= 0) {
+                const int j = base + __popc(peers & lt);
+                if (j < a.cap) row = e * a.cap + j; else overflow = true;
+                if ((peers & lt) == 0) s_count[e] = base + __popc(peers);
+            }
+            if (q < m) {
+                s_own[q] = row;
+                a.ll_slot[i_begin + q] = row;
+            }
+            __syncwarp();
         }
-        const int base = e >= 0 ? my_hist[e] : 0;
-        __syncwarp();
-        if (e >= 0 && (peers & lt) == 0) my_hist[e] = base + __popc(peers);
-        __syncwarp();
-        if (i < n) s_pos[i] = base + __popc(peers & lt);
+        if (__any_sync(0xffffffffu, overflow) && lane == 0) atomicOr(&s_flags, MOE_DEVERR_CAPACITY);
+    } else if (first) {
+        // CTA 0: the counts; any expert over capacity overflowed somewhere
+        bool over = false;
+        for (int e = tid - 32; e < a.E; e += kLLThreads - 32) {
+            a.tokens_per_expert[e] = min(s_total[e], a.cap);
+            over |= s_total[e] > a.cap;
+        }
+        if (over) atomicOr(&s_flags, MOE_DEVERR_CAPACITY);
     }
     __syncthreads();
-    // exclusive scan across the warps; totals per expert
-    for (int e = tid; e < a.E; e += kLLThreads) {
-        int run = 0;
-        for (int w = 0; w < kLLWarps; ++w) {
-            const int v = s_hist[w * a.E + e];
-            s_hist[w * a.E + e] = run;
-            run += v;
-        }
-        if (blockIdx.x == 0) a.tokens_per_expert[e] = min(run, a.cap);
-    }
-    __syncthreads();
-    bool overflow = false;
-    for (int i = tid; i < n; i += kLLThreads) {
-        const int e = s_e[i];
-        int32_t row = -1;
-        if (e >= 0) {
-            const int j = s_hist[(i / seg) * a.E + e] + s_pos[i];
-            if (j < a.cap) row = e * a.cap + j; else overflow = true;
-        }
-        s_pos[i] = row;
-        if (blockIdx.x == 0) a.ll_slot[i] = row;
-    }
-    const int flags = __syncthreads_or(bad_id) ? MOE_DEVERR_EXPERT_ID : 0;
-    const int flags2 = __syncthreads_or(overflow) ? MOE_DEVERR_CAPACITY : 0;
-    if (blockIdx.x == 0 && tid == 0) *a.status = static_cast<uint32_t>(flags | flags2);
+    if (first && tid == 0) *a.status = s_flags;
     pdl_trigger();
 
     // each token row once into registers, then out to the token's destination rows
@@ -124,7 +137,7 @@ ll_dispatch_kernel(LLArgs a) {
         for (int c0 = 0; c0 < a.H8; c0 += group) {
             if (t != t_begin || c0 != 0) load_group(a, t, c0, tid, v);
             for (int k = 0; k < a.K; ++k) {
-                const int32_t row = s_pos[t * a.K + k];          // the same for every thread
+                const int32_t row = s_own[(t - t_begin) * a.K + k];   // the same for every thread
                 if (row < 0) continue;
                 uint4* dst = a.recv + static_cast<int64_t>(row) * a.H8;
 #pragma unroll
@@ -139,7 +152,7 @@ ll_dispatch_kernel(LLArgs a) {
 
 }  // namespace
 
-int32_t ll_max_entries() { return 4096; }
+int32_t ll_max_entries() { return kLLMaxEntries; }
 
 cudaError_t launch_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32_t T, int32_t K, int32_t E,
                                int32_t hidden, int32_t cap, uint16_t* recv, int32_t* tokens_per_expert,
@@ -153,16 +166,19 @@ cudaError_t launch_ll_dispatch(const uint16_t* x, const int32_t* topk_idx, int32
     a.ll_slot = ll_slot;
     a.status = status;
     const int n = T * K;
-    const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(n) + static_cast<size_t>(kLLWarps) * E);
-    cudaError_t err = cudaFuncSetAttribute(ll_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                           static_cast<int>(smem));
-    if (err != cudaSuccess) return err;
+    if (n > kLLMaxEntries) return cudaErrorInvalidValue;     // the host checks ll_max_entries() first
     // one token per CTA, at most two CTAs per SM (then several tokens per CTA)
     int64_t grid = num_channels > 0 ? num_channels : T;
     const int64_t max_grid = static_cast<int64_t>(sm_count()) * 2;
     if (num_channels <= 0 && grid > max_grid) grid = max_grid;
     if (grid > T) grid = T;
     if (grid < 1) grid = 1;
+    // two expert counters per expert and one word per entry of the largest token range
+    const int64_t max_tokens = (static_cast<int64_t>(T) + grid - 1) / grid;
+    const size_t smem = sizeof(int32_t) * (2 * static_cast<size_t>(E) + static_cast<size_t>(max_tokens) * K);
+    cudaError_t err = cudaFuncSetAttribute(ll_dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           static_cast<int>(smem));
+    if (err != cudaSuccess) return err;
     return launch_pdl(ll_dispatch_kernel, dim3(static_cast<unsigned>(grid)), dim3(kLLThreads), smem, stream, a);
 }
 
