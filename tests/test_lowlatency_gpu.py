@@ -55,7 +55,7 @@ def test_ll_parity_decode_batches(T):
 @pytest.mark.parametrize("T,H,E,K,cap,mask,dups,seed,channels", [
     (100, 136, 16, 3, 100, 0.2, True, 1, 0),
     (300, 64, 1024, 8, 32, 0.0, False, 2, 0),
-    (200, 64, 300, 6, 64, 0.05, True, 6, 0),     # just past the lane-mask table's 256 experts: one ballot per id bit
+    (200, 64, 300, 6, 64, 0.05, True, 6, 0),     # duplicate ids with 300 experts: equal experts inside one warp chunk
     (256, 8, 4, 16, 1024, 0.1, True, 3, 7),     # few experts, many entries each
     (0, 64, 8, 2, 4, 0.0, False, 4, 0),
     (40, 9224, 16, 4, 16, 0.1, False, 5, 300),    # rows wider than one column group; more channels than tokens
