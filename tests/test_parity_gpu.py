@@ -278,3 +278,41 @@ def test_wide_dispatch_falls_back_when_only_16_byte_aligned(fmt):
             assert np.array_equal(recv[:n].cpu().numpy(), o["recv_q"])
             assert np.array_equal(np.ascontiguousarray(scales[:n].cpu().numpy()).view(np.uint8),
                                   np.ascontiguousarray(o["recv_scales"]).view(np.uint8))
+
+
+def test_wide_gathers_fall_back_when_only_16_byte_aligned():
+    """The 32-byte gather (the dispatch backward's default, the combine's
+    variant 4) needs 32-byte aligned rows; inputs and outputs at a 16-byte
+    offset take the 16-byte gather instead, with the same results."""
+    import oracle
+    from combine_moe_dispatch_02_gb300 import ep
+    from combine_moe_dispatch_02_gb300.inputs import bf16_bits
+    T, H, E, R, K = 300, 1024, 32, 8, 6
+    idx = random_routing(T, K, E, 33, mask_frac=0.05)
+    w = random_weights(T, K, 33)
+    g_ = torch.Generator().manual_seed(34)
+    L = ep.Layout(T, K, E, R)
+    ep.moe_dispatch_layout(idx.cuda(), w.cuda(), E, R, L)
+    Lo = oracle.layout(idx.numpy(), w.numpy(), E, R, None)
+    # dispatch backward: grad_recv and grad_x 16 bytes past a 32-byte boundary
+    grad_recv = (torch.randn(L.capacity, H, generator=g_) * 2).to(torch.bfloat16)
+    gr_buf = torch.empty(L.capacity * H + 8, dtype=torch.bfloat16, device="cuda")
+    gr = gr_buf[8:].view(L.capacity, H)
+    gr.copy_(grad_recv.cuda())
+    gx_buf = torch.empty(T * H + 8, dtype=torch.bfloat16, device="cuda")
+    gx = gx_buf[8:].view(T, H)
+    assert gr.data_ptr() % 32 == 16 and gx.data_ptr() % 32 == 16
+    ep.moe_dispatch_backward(gr, L, gx)
+    ox, s1 = oracle.dispatch_backward(bf16_bits(grad_recv), Lo.recv_slot)
+    assert s1 == 0 and np.array_equal(bf16_bits(gx.cpu()), ox)
+    # combine, variant 4: y and out at the same offset
+    y = torch.randn(T * K, H, generator=g_).to(torch.bfloat16)
+    y_buf = torch.empty(T * K * H + 8, dtype=torch.bfloat16, device="cuda")
+    yd = y_buf[8:].view(T * K, H)
+    yd.copy_(y.cuda())
+    out_buf = torch.empty(T * H + 8, dtype=torch.bfloat16, device="cuda")
+    out = out_buf[8:].view(T, H)
+    ep.moe_combine(yd, L, w.cuda(), out, variant=4)
+    oo, s2 = oracle.combine(bf16_bits(y), Lo.expert_slot, w.numpy())
+    assert s2 == 0 and np.array_equal(bf16_bits(out.cpu()), oo)
+    assert ep.moe_layout_read_status(L) == (0, 0)
