@@ -194,9 +194,10 @@ moe_status moe_layout_init_sources(moe_layout* L, int32_t S, int32_t source_toke
  * experts and wide expert parallelism").  Inputs: topk_idx int32 [T,K]
  * (-1 = masked) and topk_w fp32 [T,K] (may be NULL: expert_weight is then
  * zero-filled).  Two kernels: a warp-aggregated per-tile histogram with a
- * decoupled-lookback scan over E-wide count vectors (tiles claim ids from a
- * ticket so every wait is on a running CTA; every wait is bounded), then a
- * finalize pass.
+ * decoupled-lookback scan over E-wide count vectors (up to one tile per SM,
+ * the tile is the block index and all tiles are resident at once; more tiles
+ * claim ids from a ticket so every wait is on a running CTA; every wait is
+ * bounded), then a finalize pass.
  * num_experts / num_ranks must equal L->E / L->R. */
 moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w,
                                int32_t num_experts, int32_t num_ranks,

@@ -91,6 +91,8 @@ def test_combine_gather(T, H, E, R, K, mask, seed):
     (262144, 8, 256, 8, 8, 0.0, False, 20),    # 1,024 scan tiles: the flag look-back at length
     (100003, 16, 64, 4, 6, 0.05, False, 21),   # ragged last tile, masked entries
     (65536, 128, 256, 8, 8, 0.0, True, 22),    # FP8 over 256 tiles
+    (20000, 16, 256, 8, 8, 0.02, False, 23),   # 79 tiles: the flag look-back with block-index tiles
+    (8449, 32, 256, 8, 8, 0.0, False, 24),     # 34 tiles: the first count past the tagged look-back
 ])
 def test_large_token_counts(T, H, E, R, K, mask, fp8, seed):
     idx = random_routing(T, K, E, seed, mask_frac=mask)
