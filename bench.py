@@ -485,7 +485,8 @@ def run_ours(args, rank, world, local_rank):
                  "datasheet HBM3e bandwidth; the timed steps rotate over 4 independently allocated buffer sets "
                  "(step_us_by_placement: the mean of each)"),
         "step_us": pct(tot),
-        "step_us_by_placement": [round(statistics.mean(tot[i::NPLACE]) * 1e3, 2) for i in range(NPLACE)],
+        "step_us_by_placement": [round(statistics.mean(tot[i::NPLACE]) * 1e3, 2)
+                                 for i in range(min(NPLACE, len(tot)))],
         "layout": {"us": round(statistics.mean(g_lay) * 1e3, 2), "us_pct": pct(g_lay),
                    "eager_us": round(statistics.mean(lay) * 1e3, 2), "bytes": ab["layout"]},
         f"dispatch_{FORMAT_NAMES[fmt]}": hbm_op(ab[dkey], g_dis, dis, s_dis,

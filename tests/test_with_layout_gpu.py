@@ -219,3 +219,85 @@ def test_timeout_is_reported_and_recoverable():
     o = oracle_run(inp.x, inp.topk_idx, inp.topk_w, None, wl.E, wl.R, fp8=1)
     n = o["n_pairs"]
     assert np.array_equal(recv[:n].cpu().numpy(), o["recv_q"])
+
+
+def _check_layout_and_rows(L, recv, scales, x, idx, w, E, R, fmt):
+    assert ep.moe_layout_read_status(L) == (0, 0)
+    res = {f: getattr(L, f).cpu().numpy() for f in LAYOUT_FIELDS}
+    n = int(res["rank_offset"][R])
+    res["n_pairs"] = n
+    if fmt:
+        res["recv_q"] = recv[:n].cpu().numpy()
+        res["recv_scales"] = scales[:n].cpu().numpy().copy()
+    else:
+        res["recv_x"] = bf16_bits(recv[:n].cpu())
+    o = oracle_run(x, idx, w, None, E, R, fp8=fmt)
+    assert_parity(res, o, fp8=bool(fmt))
+
+
+def test_call_kinds_interleaved_on_one_layout():
+    """The one call (early loads for bf16 and MXFP8, not for FP8), the
+    separate calls, a one call on another grid (few channels) and the layout
+    alone, alternating on one workspace with new routings: every call
+    matches the oracle, so no call reads a word another call left behind."""
+    T, H, E, R, K = 1500, 1024, 64, 8, 6
+    L = ep.Layout(T, K, E, R)
+    bufs = {fmt: ep.alloc_recv(L, H, fmt) for fmt in (0, 1, 2)}
+    kinds = ["fused", "separate", "fused", "fused_channels", "fused", "layout_only", "fused", "fused"]
+    fmts = [0, 0, 1, 2, 2, 0, 0, 1]
+    for step, (kind, fmt) in enumerate(zip(kinds, fmts)):
+        seed = 900 + step
+        idx = random_routing(T, K, E, seed, mask_frac=0.05)
+        w = random_weights(T, K, seed)
+        g_ = torch.Generator().manual_seed(seed + 1)
+        x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
+        idx_d, w_d, x_d = idx.cuda(), w.cuda(), x.cuda()
+        recv, scales = bufs[fmt]
+        if kind == "fused":
+            ep.moe_dispatch_with_layout(idx_d, w_d, E, R, L, x_d, fmt, recv, scales)
+        elif kind == "fused_channels":
+            ep.moe_dispatch_with_layout(idx_d, w_d, E, R, L, x_d, fmt, recv, scales, num_channels=40)
+        elif kind == "separate":
+            ep.moe_dispatch_layout(idx_d, w_d, E, R, L)
+            ep.moe_dispatch(x_d, L, fmt, recv, scales)
+        else:
+            ep.moe_dispatch_layout(idx_d, w_d, E, R, L)
+            assert ep.moe_layout_read_status(L) == (0, 0)
+            o = oracle_run(x, idx, w, None, E, R, fp8=0)
+            assert np.array_equal(L.recv_slot.cpu().numpy().ravel(), o["recv_slot"].ravel())
+            continue
+        _check_layout_and_rows(L, recv, scales, x, idx, w, E, R, fmt)
+
+
+@pytest.mark.parametrize("T", [20000, 40000])
+@pytest.mark.parametrize("fmt", [0, 1, 2])
+def test_many_scan_tiles(T, fmt):
+    """79 scan tiles (flag look-back, tiles by block index) and 157 (more
+    than the SMs: tiles from the ticket) in the one call."""
+    H, E, R, K = 256, 256, 8, 8
+    idx = random_routing(T, K, E, 41, mask_frac=0.02)
+    w = random_weights(T, K, 41)
+    g_ = torch.Generator().manual_seed(42)
+    x = (torch.randn(T, H, generator=g_) * 2).to(torch.bfloat16)
+    L = ep.Layout(T, K, E, R)
+    assert L.c.num_tiles in (79, 157)
+    recv, scales = ep.alloc_recv(L, H, fmt)
+    ep.moe_dispatch_with_layout(idx.cuda(), w.cuda(), E, R, L, x.cuda(), fmt, recv, scales)
+    _check_layout_and_rows(L, recv, scales, x, idx, w, E, R, fmt)
+
+
+@pytest.mark.parametrize("fmt", [0, 2])
+def test_timeout_is_reported_and_recoverable_bf16_mx(fmt):
+    """As above for the formats whose dispatch loads early (its grid is
+    resident while the scan gives up)."""
+    wl = WORKLOADS["dsv3"].scaled(2048)
+    inp = make_inputs(wl, with_y=False)
+    L = ep.Layout(2048, wl.K, wl.E, wl.R)
+    recv, scales = ep.alloc_recv(L, wl.H, fmt)
+    idx, w, x = inp.topk_idx.cuda(), inp.topk_w.cuda(), inp.x.cuda()
+    ep.moe_dispatch_with_layout(idx, w, wl.E, wl.R, L, x, fmt, recv, scales, wait_timeout_ns=20_000_000,
+                                debug_flags=ep.MOE_DEBUG_STALL_FIRST_TILE)
+    st, flags = ep.moe_layout_read_status(L)
+    assert st == ep.MOE_ERR_TIMEOUT and flags & ep.MOE_DEVERR_TIMEOUT
+    ep.moe_dispatch_with_layout(idx, w, wl.E, wl.R, L, x, fmt, recv, scales)
+    _check_layout_and_rows(L, recv, scales, inp.x, inp.topk_idx, inp.topk_w, wl.E, wl.R, fmt)
