@@ -72,6 +72,8 @@ struct ScanArgs {
 // a multiple of 4 so that the look-back can move it in 16-byte pieces.
 __host__ __device__ __forceinline__ int vec_width(int E) { return (2 * E + 3) / 4 * 4; }
 
+__host__ __device__ __forceinline__ int round_up4(int n) { return (n + 3) / 4 * 4; }
+
 // Key of a valid entry: (rank << 16) | expert (experts < 2^16); -1 if masked.
 // Two keys share a rank iff their upper halves are equal, and then compare like
 // their expert ids.
@@ -141,9 +143,10 @@ layout_scan_kernel(ScanArgs a) {
     int32_t* s_agg = s_prefix + W;                                    // [W]
     int4* s_part = reinterpret_cast<int4*>(s_agg + W);                // [kLayoutThreads]
     int32_t* s_rank = reinterpret_cast<int32_t*>(s_part + kLayoutThreads);   // [E]
-    int32_t* s_min = s_rank + a.E;    // [tile_tokens][R] if prim_table: min of (e << 5 | k) per (token, rank)
+    // [tile_tokens][R] if prim_table: min of (e << 5 | k) per (token, rank)
+    int32_t* s_min = s_rank + round_up4(a.E);
     const bool peer_table = a.E <= kMaxPeerE;
-    uint32_t* s_peer = reinterpret_cast<uint32_t*>(s_min + (a.prim_table ? a.tile_tokens * a.R : 0));   // [warps][kMaxPeerE]
+    uint32_t* s_peer = reinterpret_cast<uint32_t*>(s_min + (a.prim_table ? round_up4(a.tile_tokens * a.R) : 0));   // [warps][kMaxPeerE]
     __shared__ int s_tile;
     __shared__ uint32_t s_gen;
     __shared__ int s_lb_count, s_lb_final;
@@ -157,7 +160,12 @@ layout_scan_kernel(ScanArgs a) {
     // as they all fit at once).  Otherwise the tile comes from the ticket.
     constexpr int kIdsPerThread = kMaxTileEntries / kLayoutThreads;
     int32_t e_in[kIdsPerThread];
-    uint32_t epoch0 = 0;    // by_block: the call counter (thread 0), needed at the publish
+    // by_block: the call counter, needed at the publish.  Every thread loads
+    // it, unconditionally: a load's result merged at the end of a one-thread
+    // branch made that thread wait for it there (0.6 us, with the whole CTA
+    // behind it at the next barrier).  The previous call's finalize wrote it
+    // and has completed (the dependency wait above).
+    const uint32_t epoch0 = __ldcg(&a.ws.hdr->epoch);
     if (a.by_block) {
         const int64_t base = static_cast<int64_t>(blockIdx.x) * a.tile_tokens * a.K;
         const int nn = min(a.tile_tokens, a.T - static_cast<int>(blockIdx.x) * a.tile_tokens) * a.K;
@@ -166,18 +174,22 @@ layout_scan_kernel(ScanArgs a) {
             const int i = tid + u * kLayoutThreads;
             e_in[u] = i < nn ? __ldg(a.topk_idx + base + i) : -1;
         }
-        if (tid == 0) epoch0 = ld_relaxed_gpu(&a.ws.hdr->epoch);
     } else if (tid == 0) {
         s_tile = static_cast<int>(atomicAdd(&a.ws.hdr->ticket, 1u));
         s_gen = (ld_relaxed_gpu(&a.ws.hdr->epoch) & kGenMask) + 1u;
     }
-    for (int i = tid; i < kLayoutWarps * W; i += kLayoutThreads) s_hist[i] = 0;
-    for (int i = tid; i < W; i += kLayoutThreads) s_agg[i] = 0;
+    // shared-memory set-up in 16-byte stores (every table starts on a 16-byte
+    // boundary; W is a multiple of 4)
+    for (int i = tid; i < kLayoutWarps * W / 4; i += kLayoutThreads)
+        reinterpret_cast<int4*>(s_hist)[i] = make_int4(0, 0, 0, 0);
+    for (int i = tid; i < W / 4; i += kLayoutThreads) reinterpret_cast<int4*>(s_agg)[i] = make_int4(0, 0, 0, 0);
     for (int e = tid; e < a.E; e += kLayoutThreads) s_rank[e] = e / a.m;
     if (a.prim_table)
-        for (int i = tid; i < a.tile_tokens * a.R; i += kLayoutThreads) s_min[i] = INT_MAX;
+        for (int i = tid; i < round_up4(a.tile_tokens * a.R) / 4; i += kLayoutThreads)
+            reinterpret_cast<int4*>(s_min)[i] = make_int4(INT_MAX, INT_MAX, INT_MAX, INT_MAX);
     if (peer_table)
-        for (int i = tid; i < kLayoutWarps * kMaxPeerE; i += kLayoutThreads) s_peer[i] = 0u;
+        for (int i = tid; i < kLayoutWarps * kMaxPeerE / 4; i += kLayoutThreads)
+            reinterpret_cast<uint4*>(s_peer)[i] = make_uint4(0u, 0u, 0u, 0u);
     __syncthreads();
     const int tile = a.by_block ? static_cast<int>(blockIdx.x) : s_tile;
     if (tile >= a.num_tiles) return;   // cannot happen: one CTA per tile
@@ -371,12 +383,15 @@ layout_scan_kernel(ScanArgs a) {
             int32_t sum = 0;
             for (int q0 = 0; q0 < tile && !tmo && !aborted; q0 += kTaggedBatch) {
                 uint64_t v[kTaggedBatch];
+                // every load unconditional (index clamped, the extra words
+                // ignored below): a load under a condition made the thread
+                // wait for it before issuing the next one
 #pragma unroll
                 for (int u = 0; u < kTaggedBatch; ++u)
-                    v[u] = q0 + u < tile ? ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(q0 + u) * W + col)
-                                         : (static_cast<uint64_t>(gen) << 32);
+                    v[u] = ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(min(q0 + u, tile - 1)) * W + col);
 #pragma unroll
                 for (int u = 0; u < kTaggedBatch; ++u) {
+                    if (q0 + u >= tile) break;
                     uint64_t t0 = 0;
                     for (uint32_t it = 0; static_cast<uint32_t>(v[u] >> 32) != gen; ++it) {
                         if (ld_relaxed_gpu(&a.ws.hdr->abort) == gen) { aborted = true; break; }
@@ -591,9 +606,11 @@ layout_finalize_kernel(FinalArgs a) {
     }
     for (int i = tid; i < a.E; i += kFinalizeThreads) s_rank[i] = i / a.m;
     for (int i = tid; i < nt * a.R; i += kFinalizeThreads) s_rs[i] = -1;
-    // the call counter only changes in this kernel (block 0, below)
+    // the call counter only changes in this kernel (block 0, below); the
+    // header words are loaded by every thread, unconditionally, so that no
+    // thread waits for them before it uses them
     const bool header = blockIdx.x == 0 && tid == 0;
-    const uint32_t epoch = header ? ld_relaxed_gpu(&a.ws.hdr->epoch) : 0u;
+    const uint32_t epoch = __ldcg(&a.ws.hdr->epoch);
 
     pdl_wait();
     if (!a.early_trigger) pdl_trigger();    // one wave of CTAs: the dispatch grid may become resident now
@@ -606,7 +623,7 @@ layout_finalize_kernel(FinalArgs a) {
         er_r[u] = i < n ? __ldcg(a.ws.erank + e0 + i) : 0;
         pr_r[u] = i < n ? __ldcg(a.ws.prank + e0 + i) : 0;
     }
-    const uint32_t k1 = header ? ld_relaxed_gpu(&a.ws.hdr->k1_err) : 0u;   // the scan's error bits
+    const uint32_t k1 = __ldcg(&a.ws.hdr->k1_err);   // the scan's error bits (used by the header thread)
     const int32_t* totals = a.ws.tile_incl + static_cast<int64_t>(a.num_tiles - 1) * vec_width(a.E);
     expert_offsets(totals, a.E, s_eoff, s_poff, s_warp);
 #pragma unroll
@@ -824,9 +841,9 @@ cudaError_t launch_layout(const int32_t* topk_idx, const float* topk_w, const mo
     sa.by_block = L->num_tiles <= device_sm_count() ? 1 : 0;
     const bool src = L->num_sources > 0;
     size_t smem1 = sizeof(int32_t) * (kMaxTileEntries + (kLayoutWarps + 2) * static_cast<size_t>(vec_width(L->E)) +
-                                      static_cast<size_t>(L->E)) + sizeof(int4) * kLayoutThreads;
+                                      static_cast<size_t>(round_up4(L->E))) + sizeof(int4) * kLayoutThreads;
     if (L->E <= kMaxPeerE) smem1 += sizeof(uint32_t) * kLayoutWarps * kMaxPeerE;   // lane-mask tables
-    const size_t table_bytes = sizeof(int32_t) * static_cast<size_t>(L->tile_tokens) * L->R;
+    const size_t table_bytes = sizeof(int32_t) * static_cast<size_t>(round_up4(L->tile_tokens * L->R));
     sa.prim_table = (static_cast<int64_t>(L->tile_tokens) * L->R <= kMaxPrimSlots &&
                      smem1 + table_bytes <= kMaxSmemPerBlock) ? 1 : 0;
     if (sa.prim_table) smem1 += table_bytes;
