@@ -52,6 +52,8 @@ def test_workload_parity_full_size(name):
     (700, 256, 128, 64, 8, 0.1, False, True, 12),   # FP8 with more than 32 destination ranks
     (300, 48, 16, 4, 4, 0.0, False, False, 13),      # bf16 rows ending half-way through a 32-column lane
     (257, 3200, 16, 8, 4, 0.05, False, True, 14),    # FP8 rows ending inside a 1024-column segment
+    (250, 64, 6, 3, 5, 0.1, False, False, 15),       # E and tile_tokens * R (1227) not multiples of 4:
+                                                     # the scan's padded shared-memory tables
 ])
 @pytest.mark.parametrize("variant", [1, 2, 3, 4])
 def test_edge_case_parity(T, H, E, R, K, mask, dups, fp8, seed, variant):
