@@ -14,8 +14,8 @@ pytestmark = pytest.mark.gpu
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
-def _run(*extra):
-    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "5", "--warmup", "3",
+def _run(*extra, steps=5):
+    cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--steps", str(steps), "--warmup", "3",
            "--no-cpu-baseline", *extra]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, r.stderr[-3000:]
@@ -80,3 +80,11 @@ def test_bench_fp8_step_and_format_legs():
     # the step's bytes: layout + FP8 dispatch + combine
     step_bytes = ops["layout"]["bytes"] + 218_836_384 + d["roofline"]["algorithmic_bytes"]
     assert abs(d["value"] * 1e9 * d["ms_per_step"] * 1e-3 / step_bytes - 1) < 1e-3
+
+
+def test_bench_fewer_steps_than_buffer_placements():
+    """The timed steps rotate over four buffer placements; three steps
+    (the launch-list profile's command) report the three placements timed."""
+    d = _run("--legs", "none", steps=3)
+    assert d["steps"] == 3 and d["value"] > 0
+    assert len(d["ops"]["step_us_by_placement"]) == 3
