@@ -161,10 +161,11 @@ layout_scan_kernel(ScanArgs a) {
     constexpr int kIdsPerThread = kMaxTileEntries / kLayoutThreads;
     int32_t e_in[kIdsPerThread];
     // by_block: the call counter, needed at the publish.  Every thread loads
-    // it, unconditionally: a load's result merged at the end of a one-thread
-    // branch made that thread wait for it there (0.6 us, with the whole CTA
-    // behind it at the next barrier).  The previous call's finalize wrote it
-    // and has completed (the dependency wait above).
+    // it, unconditionally: loaded by thread 0 inside a branch of its own, it
+    // held that thread for a memory round trip right there (0.6 us measured
+    // on GB300), and the whole CTA behind it at the next barrier.  The
+    // previous call's finalize wrote it and has completed (the dependency
+    // wait above).
     const uint32_t epoch0 = __ldcg(&a.ws.hdr->epoch);
     if (a.by_block) {
         const int64_t base = static_cast<int64_t>(blockIdx.x) * a.tile_tokens * a.K;
