@@ -109,6 +109,23 @@ constexpr uint32_t kWaitTimedOut = 4u;
 constexpr int kLookbackWindow = 32;      // predecessors one look-back step inspects (warp 0's lanes)
 constexpr int kTaggedBatch = 16;         // tagged words a thread loads at once (one round for <= 16 predecessors)
 
+// Threads that share a column of the tagged look-back: the largest power of
+// two g <= 32 with g * W <= kLayoutThreads (1 where W > kLayoutThreads / 2).
+// The g threads of a column are adjacent lanes of one warp.
+__host__ __device__ __forceinline__ int lookback_group(int W) {
+    int g = 1;
+    while (g < 32 && 2 * g * W <= kLayoutThreads) g *= 2;
+    return g;
+}
+
+// Tiles up to which the look-back uses generation-tagged aggregates: every
+// look-back then sums all its predecessors, in at most two rounds of loads
+// per thread (one round once kTaggedBatch * g covers them).
+__host__ __device__ __forceinline__ int tagged_tile_limit(int E) {
+    const int g = lookback_group(vec_width(E));
+    return kTaggedBatch * g + 1 > kLookbackWindow + 1 ? kTaggedBatch * g + 1 : kLookbackWindow + 1;
+}
+
 // Wait (bounded) until a tile flag carries generation `gen`; return its state,
 // kFlagError if another CTA aborted the scan, or kWaitTimedOut.
 __device__ uint32_t wait_tile_flag(const uint32_t* flag, uint32_t gen, const uint32_t* abort_word,
@@ -260,12 +277,13 @@ layout_scan_kernel(ScanArgs a) {
     // 1c. publish the tile aggregate now, so that successors find it on their
     //     first look-back poll; tile 0's aggregate is its inclusive prefix
     const bool stall = (a.debug_flags & MOE_DEBUG_STALL_FIRST_TILE) && tile == 0;
-    // With at most 33 tiles every look-back sums all its predecessors'
-    // aggregates, published as generation-tagged 64-bit words: no fence, no
-    // flag, and a reader validates each word it loads.  More tiles: vectors
-    // plus a progress flag (the barrier orders every thread's stores before
-    // thread 0's fence and release store, which publish them at GPU scope).
-    const bool tagged = a.num_tiles <= kLookbackWindow + 1;
+    // Up to tagged_tile_limit(E) tiles (33; 65 for E <= 64) every look-back
+    // sums all its predecessors' aggregates, published as generation-tagged
+    // 64-bit words: no fence, no flag, and a reader validates each word it
+    // loads.  More tiles: vectors plus a progress flag (the barrier orders
+    // every thread's stores before thread 0's fence and release store, which
+    // publish them at GPU scope).
+    const bool tagged = a.num_tiles <= tagged_tile_limit(a.E);
     if (tagged) {
         uint64_t* my_words = a.ws.tile_tagged + static_cast<int64_t>(tile) * W;
         if (!stall)
@@ -377,22 +395,29 @@ layout_scan_kernel(ScanArgs a) {
     //    prefixes
     bool failed = false;
     if (tile > 0 && tagged) {
-        // every thread sums its own columns over all predecessors: one round of
-        // loads, a bounded re-load of any word whose tag is not yet current
+        // g threads share a column, each summing every g-th predecessor: one
+        // round of loads for up to kTaggedBatch * g predecessors, a bounded
+        // re-load of any word whose tag is not yet current; the g partial
+        // sums meet by shuffles (every thread of a column reaches them, also
+        // after a timeout, which discards the sums)
+        const int g = lookback_group(W);
+        const int sub = tid & (g - 1);
+        const uint32_t gmask = g == 32 ? 0xffffffffu : ((1u << g) - 1u) << (lane & ~(g - 1));
         bool tmo = false, aborted = false;
-        for (int col = tid; col < W && !tmo && !aborted; col += kLayoutThreads) {
+        for (int col = tid / g; col < W && !tmo && !aborted; col += kLayoutThreads / g) {
             int32_t sum = 0;
-            for (int q0 = 0; q0 < tile && !tmo && !aborted; q0 += kTaggedBatch) {
+            for (int q0 = sub; q0 < tile && !tmo && !aborted; q0 += kTaggedBatch * g) {
                 uint64_t v[kTaggedBatch];
                 // every load unconditional (index clamped, the extra words
                 // ignored below): a load under a condition made the thread
                 // wait for it before issuing the next one
 #pragma unroll
                 for (int u = 0; u < kTaggedBatch; ++u)
-                    v[u] = ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(min(q0 + u, tile - 1)) * W + col);
+                    v[u] = ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(min(q0 + u * g, tile - 1)) * W + col);
 #pragma unroll
                 for (int u = 0; u < kTaggedBatch; ++u) {
-                    if (q0 + u >= tile) break;
+                    const int q = q0 + u * g;
+                    if (q >= tile) break;
                     uint64_t t0 = 0;
                     for (uint32_t it = 0; static_cast<uint32_t>(v[u] >> 32) != gen; ++it) {
                         if (ld_relaxed_gpu(&a.ws.hdr->abort) == gen) { aborted = true; break; }
@@ -403,13 +428,14 @@ layout_scan_kernel(ScanArgs a) {
                             break;
                         }
                         __nanosleep(it < 32 ? 32 : 256);
-                        v[u] = ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(q0 + u) * W + col);
+                        v[u] = ld_relaxed_gpu_u64(a.ws.tile_tagged + static_cast<int64_t>(q) * W + col);
                     }
                     if (tmo || aborted) break;
                     sum += static_cast<int32_t>(static_cast<uint32_t>(v[u]));
                 }
             }
-            s_prefix[col] = sum;
+            for (int d = 1; d < g; d <<= 1) sum += __shfl_xor_sync(gmask, sum, d);
+            if (sub == 0) s_prefix[col] = sum;
         }
         if (tmo) {
             atomicOr(&a.ws.hdr->k1_err, MOE_DEVERR_TIMEOUT);
@@ -497,7 +523,7 @@ layout_scan_kernel(ScanArgs a) {
     // 6. the inclusive prefix.  The last tile's is the totals vector the
     //    finalize pass reads (kernel completion publishes it).  Other tiles
     //    publish theirs, with a flag, only when look-backs use flags (more
-    //    than 33 tiles).
+    //    tiles than tagged_tile_limit(E)).
     const bool flagged = !tagged && tile > 0;     // (with flags, tile 0 published its prefix above)
     if (flagged || tile == a.num_tiles - 1) {
         int32_t* my_incl = a.ws.tile_incl + static_cast<int64_t>(tile) * W;
@@ -791,7 +817,7 @@ size_t layout_workspace_bytes(int32_t T, int32_t K, int32_t E, int32_t num_tiles
     b = align_up(b + sizeof(uint32_t) * num_tiles, 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * vec_width(E), 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(num_tiles) * vec_width(E), 256);
-    b = align_up(b + sizeof(uint64_t) * static_cast<size_t>(min(num_tiles, kLookbackWindow + 1)) * vec_width(E), 256);
+    b = align_up(b + sizeof(uint64_t) * static_cast<size_t>(min(num_tiles, tagged_tile_limit(E))) * vec_width(E), 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
     b = align_up(b + sizeof(int32_t) * static_cast<size_t>(T) * K, 256);
     return b;
@@ -810,7 +836,7 @@ LayoutWs layout_workspace(const moe_layout* L) {
     ws.tile_incl = reinterpret_cast<int32_t*>(p + off);
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->num_tiles) * vec_width(L->E), 256);
     ws.tile_tagged = reinterpret_cast<uint64_t*>(p + off);
-    off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(min(L->num_tiles, kLookbackWindow + 1)) *
+    off = align_up(off + sizeof(uint64_t) * static_cast<size_t>(min(L->num_tiles, tagged_tile_limit(L->E))) *
                              vec_width(L->E), 256);
     ws.erank = reinterpret_cast<int32_t*>(p + off);
     off = align_up(off + sizeof(int32_t) * static_cast<size_t>(L->T) * L->K, 256);

@@ -36,8 +36,9 @@ struct LayoutWs {
     uint32_t* tile_flag;   // [num_tiles]: (generation << 2) | state
     int32_t*  tile_agg;    // [num_tiles][2E]: this tile's counts (expert, primary)
     int32_t*  tile_incl;   // [num_tiles][2E]: counts of tiles 0..i inclusive
-    uint64_t* tile_tagged; // [min(num_tiles, 33)][2E]: (generation << 32) | count, the aggregates
-                           // of the look-back without flags (at most 33 tiles)
+    uint64_t* tile_tagged; // [min(num_tiles, tagged limit)][2E]: (generation << 32) | count, the
+                           // aggregates of the look-back without flags (up to 33 tiles, or 16
+                           // per thread sharing a column: 65 for E <= 64, 129 for E <= 32)
     int32_t*  erank;       // [T*K]: rank of entry among entries of its expert
     int32_t*  prank;       // [T*K]: rank of a primary entry among its expert's primaries
 };

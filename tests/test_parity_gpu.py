@@ -320,3 +320,35 @@ def test_wide_gathers_fall_back_when_only_16_byte_aligned():
     oo, s2 = oracle.combine(bf16_bits(y), Lo.expert_slot, w.numpy())
     assert s2 == 0 and np.array_equal(bf16_bits(out.cpu()), oo)
     assert ep.moe_layout_read_status(L) == (0, 0)
+
+
+@pytest.mark.parametrize("T,E,R,K,tiles", [
+    (12000, 32, 8, 8, 47),      # E = 32: eight threads share a column of the tagged look-back
+    (30000, 32, 4, 8, 118),
+    (32900, 32, 8, 8, 129),     # the last tile count of the tagged look-back for E <= 32
+    (33000, 32, 8, 8, 129),
+    (33100, 32, 8, 8, 130),     # one more: progress flags
+    (16640, 64, 8, 8, 65),      # E = 64: four threads share a column; 65 tiles tagged
+    (16641, 64, 8, 8, 66),      # 66: progress flags
+])
+def test_lookback_tile_counts(T, E, R, K, tiles):
+    """Layouts whose scan tiles sum their predecessors with several threads
+    per column (few experts), up to and past the last tile count of the
+    tagged look-back, against the oracle."""
+    import oracle
+    from combine_moe_dispatch_02_gb300 import ep
+    from harness import LAYOUT_FIELDS
+    idx = random_routing(T, K, E, T, mask_frac=0.03)
+    w = random_weights(T, K, T)
+    L = ep.Layout(T, K, E, R)
+    assert L.c.num_tiles == tiles
+    ep.moe_dispatch_layout(idx.cuda(), w.cuda(), E, R, L)
+    assert ep.moe_layout_read_status(L) == (0, 0)
+    o = oracle.layout(idx.numpy(), w.numpy(), E, R, None)
+    for f in LAYOUT_FIELDS:
+        got = getattr(L, f).cpu().numpy().ravel()
+        want = np.asarray(getattr(o, f)).ravel()
+        if f == "expert_weight":
+            assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), f
+        else:
+            assert np.array_equal(got, want), f
