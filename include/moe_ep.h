@@ -218,8 +218,8 @@ moe_status moe_dispatch_layout(const int32_t* topk_idx, const float* topk_w,
  * The scan workspace is a device array of MOE_NOALLOC_SCRATCH_BYTES compiled
  * into the library; every GPU that loads the library holds it until the
  * process exits.  Sizes whose workspace does not fit (moe_layout_bytes minus
- * the outputs; about 8 * T * K bytes plus 16 * E bytes per 2048-entry tile)
- * return MOE_ERR_UNSUPPORTED.
+ * the outputs; about 8 * T * K bytes plus 16 * E to 32 * E bytes per
+ * 2048-entry tile) return MOE_ERR_UNSUPPORTED.
  *
  * Fields of *L that are read: T, K, E, R, capacity (>= T * min(K, R)), the
  * ten output pointers and status, all caller-owned device memory of the sizes
