@@ -819,6 +819,21 @@ def run_e2e(args, inp, L, dev, fmt, step_bytes):
 
     run(max(3, args.warmup))
     torch.cuda.synchronize(dev)
+
+    def link_gbs(dst, src):
+        # one plain copy between the pinned host buffers and device memory,
+        # the median of three (the host link's rate in this process)
+        ts = []
+        for _ in range(3):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(comp)
+            dst.copy_(src, non_blocking=True)
+            b.record(comp)
+            torch.cuda.synchronize(dev)
+            ts.append(a.elapsed_time(b))
+        return round(src.numel() * src.element_size() / (statistics.median(ts) * 1e-3) / 1e9, 1)
+
+    link = {"h2d_gbs": link_gbs(bufs[0]["y"], hy), "d2h_gbs": link_gbs(hout, out)}
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(comp)
     copy.wait_event(e0)
@@ -834,7 +849,9 @@ def run_e2e(args, inp, L, dev, fmt, step_bytes):
     d2h = hout.numel() * 2 + hcnt.numel() * 4
     return {"value": round(step_bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "ms_per_step": round(ms, 4),
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": n,
-            "overlap": "inputs of step i+1 copied while step i computes (two device buffer sets)"}
+            "overlap": "inputs of step i+1 copied while step i computes (two device buffer sets)",
+            "link": link | {"note": "one plain copy of y host -> device and of out device -> host before the "
+                                    "timed steps, this process"}}
 
 
 # ------------------------------------------------------------ CPU baselines
